@@ -1,0 +1,504 @@
+#!/usr/bin/env python
+"""Benchmark of the INT4 W4A16 group-32 GEMM library on GB300.
+
+Headline workload (one "step"): the fused gate/up SwiGLU projection of a dense Kimi-K2-class MLP
+in decode / draft-tree verify, K = 7168, N = 2 x 18432, run once for each of M = 1, 4 and 16
+rows (three launches, each streaming all 165.15 MB of packed weights and scales). Metric: packed
+weight + scale bytes streamed from HBM per second (GB/s), and its fraction of the measured HBM
+copy bandwidth.
+
+Timing: W warm-up steps, then K timed steps bracketed by a barrier and a device synchronize,
+CUDA events on the launching stream, max over ranks. Each launch reads a different one of
+four weight copies (660 MB in total, > 5x the 129 MB L2), so no launch finds its weights in L2.
+SM clocks are sampled with nvidia-smi during the timed region.
+
+Also reported, outside the step: the down projection (K=18432, N=7168), the routed MoE block
+(T=64, E=384, top-8), the large-M bf16 contraction and the tiny case; the end-to-end rate
+through the public API with host buffers; the CPU oracle on a bounded sample.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "w4a16_gemm weight-HBM GB/s (% of GB300 peak) at M<=16; TFLOP/s at M=4096"
+UNIT = "GB/s"
+WORKLOAD = "dense SwiGLU gate+up decode, M in {1,4,16}, K=7168, N=2x18432, group=32"
+M_LIST = (1, 4, 16)
+N_COPIES = 4
+BYTES_PER_WEIGHT = 0.625   # 0.5 B of packed code + 4 B scale / 32 weights
+
+
+def _peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- distributed
+
+def dist_setup(gpus: int):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- ncu traffic
+
+def _kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int4_w4a16_group_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def _ncu_traffic(name: str):
+    """DRAM bytes per launch recorded from an ncu capture (profiles/<name>.json), or None when
+    there is none or the kernel sources changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", name + ".json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != _kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ----------------------------------------------------------------------------- workloads (ours)
+
+def _quantized_copies(w4, K, N, n_copies, seed, outliers=False):
+    import synth
+    copies = []
+    for c in range(n_copies):
+        W = synth.cuda_weights(K, N, seed=seed + c, outliers=outliers)
+        copies.append(w4.w4a16_quantize(W))
+        del W
+    return copies
+
+
+def _time_launches(stream, fns):
+    """Runs fns in order on `stream` with an event between consecutive calls; returns the
+    per-call device times in ms (after synchronizing)."""
+    import torch
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+    # Hold the stream for a few ms so the host enqueues every call before the first one runs:
+    # the measured intervals are then device time, not host launch gaps.
+    torch.cuda._sleep(int(20e6))
+    ev[0].record(stream)
+    for i, fn in enumerate(fns):
+        fn()
+        ev[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(fns))]
+
+
+def run_ours(args, rank, world):
+    import torch
+    import int4_w4a16_group_gb300 as w4
+    import synth
+
+    peaks = _peaks()
+    stream = torch.cuda.current_stream()
+    K, I = synth.SWIGLU["K"], synth.SWIGLU["I"]
+    N = 2 * I
+    weights = _quantized_copies(w4, K, N, N_COPIES, seed=1000 + 17 * rank)
+    xs = {M: synth.cuda_normal((M, K), 1.0, seed=rank, stream=M) for M in M_LIST}
+    ys = {M: torch.empty((M, I), dtype=torch.float32, device="cuda") for M in M_LIST}
+    launches_per_step = sum((M + 15) // 16 for M in M_LIST)
+    wbytes = BYTES_PER_WEIGHT * K * N
+    state = {"i": 0}
+
+    def step_fns():
+        fns = []
+        for M in M_LIST:
+            def f(M=M):
+                qw, sc = weights[state["i"] % N_COPIES]
+                state["i"] += 1
+                w4.w4a16_gemm_swiglu(xs[M], qw, sc, ys[M], stream=stream)
+            fns.append(f)
+        return fns
+
+    for _ in range(args.warmup):
+        for f in step_fns():
+            f()
+    torch.cuda.synchronize()
+
+    per_launch = {M: [] for M in M_LIST}
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        fns = []
+        for _ in range(args.steps):
+            fns.extend(step_fns())
+        times = _time_launches(stream, fns)
+        barrier(world)
+        torch.cuda.synchronize()
+    clocks = clk.summary()
+    total_ms = sum(times)
+    for i, t in enumerate(times):
+        per_launch[M_LIST[i % len(M_LIST)]].append(t)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps * len(M_LIST) * wbytes / (total_ms * 1e-3) / 1e9
+
+    avg_launch_ms = sum(times) / len(times)
+    achieved = wbytes / (avg_launch_ms * 1e-3) / 1e9
+    per_m = {str(M): {"us": 1e3 * statistics.mean(per_launch[M]),
+                      "GB/s": wbytes / (statistics.mean(per_launch[M]) * 1e-3) / 1e9,
+                      "frac_of_hbm": wbytes / (statistics.mean(per_launch[M]) * 1e-3) / 1e9 / peaks["hbm_gbs"]}
+             for M in M_LIST}
+
+    # end to end through the public API: pinned host x in, host y out, every step
+    xh = {M: torch.empty((M, K), dtype=torch.float32, pin_memory=True).copy_(xs[M].cpu()) for M in M_LIST}
+    yh = {M: torch.empty((M, I), dtype=torch.float32, pin_memory=True) for M in M_LIST}
+    xd = {M: torch.empty((M, K), dtype=torch.float32, device="cuda") for M in M_LIST}
+
+    def e2e_step():
+        for M in M_LIST:
+            qw, sc = weights[state["i"] % N_COPIES]
+            state["i"] += 1
+            xd[M].copy_(xh[M], non_blocking=True)
+            w4.w4a16_gemm_swiglu(xd[M], qw, sc, ys[M], stream=stream)
+            yh[M].copy_(ys[M], non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(2):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    e2e = {"value": world * args.steps * len(M_LIST) * wbytes / e2e_s / 1e9, "unit": UNIT,
+           "h2d_bytes_per_step": sum(M * K * 4 for M in M_LIST),
+           "d2h_bytes_per_step": sum(M * I * 4 for M in M_LIST)}
+    del weights
+
+    out = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded N(0,0.02) weights quantized on the device, N(0,1) activations)",
+        "config": {"workload": WORKLOAD, "M": list(M_LIST), "K": K, "N": N, "group": 32,
+                   "launches_per_step": launches_per_step, "parallelism": f"replicas x{world}",
+                   "l2": f"each launch reads one of {N_COPIES} weight copies "
+                         f"({N_COPIES * wbytes / 1e6:.0f} MB > 129 MB L2)"},
+        "per_M": per_m,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": _ncu_traffic("gemv_swiglu_k7168_n36864"),
+                     "kernel": "w4a16 small-M weight-streaming GEMM (fused SwiGLU)",
+                     "algorithmic_bytes_per_launch": wbytes,
+                     "peak_source": peaks["source"] + " hbm_gbs (copy)"},
+        "clocks": clocks,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * args.steps,
+    }
+    if not args.no_breakdown:
+        out["other_workloads"] = other_workloads(args, w4, peaks, stream)
+    return out
+
+
+def other_workloads(args, w4, peaks, stream):
+    """Down projection, routed MoE, large-M bf16 and tiny: each timed on its own (not part of
+    the step), device time per launch with CUDA events, after warm-up."""
+    import torch
+    import synth
+    res = {}
+    reps = max(5, args.steps)
+
+    # down projection, M in {1,4,16}: 4 rotating weight copies (330 MB)
+    K, N = synth.DOWN["K"], synth.DOWN["N"]
+    wb = BYTES_PER_WEIGHT * K * N
+    copies = _quantized_copies(w4, K, N, N_COPIES, seed=2000, outliers=True)
+    down = {}
+    for M in M_LIST:
+        x = synth.cuda_normal((M, K), synth.DOWN_X_STD, seed=7, stream=M)
+        y = torch.empty((M, N), dtype=torch.float32, device="cuda")
+        fns = [lambda c=c: w4.w4a16_gemm(x, copies[c % N_COPIES][0], copies[c % N_COPIES][1], y,
+                                         stream=stream) for c in range(reps + 3)]
+        t = _time_launches(stream, fns)[3:]
+        us = 1e3 * statistics.mean(t)
+        down[str(M)] = {"us": us, "GB/s": wb / (us * 1e-6) / 1e9,
+                        "frac_of_hbm": wb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    res["down_K18432_N7168"] = down
+    del copies
+
+    # routed MoE, T=64 draft-tree rows, 384 experts, top-8
+    c = synth.MOE
+    T, E, topk, K, I = c["T"], c["E"], c["topk"], c["K"], c["I"]
+    gq = torch.empty((E, K // 8, 2 * I), dtype=torch.int32, device="cuda")
+    gs = torch.empty((E, K // 32, 2 * I), dtype=torch.float32, device="cuda")
+    dq = torch.empty((E, I // 8, K), dtype=torch.int32, device="cuda")
+    ds = torch.empty((E, I // 32, K), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        a, b = synth.cuda_moe_expert_weights(e, K, I, seed=0)
+        w4.w4a16_quantize(a, gq[e], gs[e])
+        w4.w4a16_quantize(b, dq[e], ds[e])
+        del a, b
+    ids, logits = synth.routing(T, E, topk, seed=0)
+    active = len(np.unique(ids))
+    x = synth.cuda_normal((T, K), 1.0, seed=0, stream=5)
+    idd = torch.from_numpy(ids).cuda()
+    wts = w4.w4a16_topk_softmax(torch.from_numpy(logits).cuda())
+    out = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    ws = torch.empty(w4.w4a16_moe_workspace_size(T, topk, E, K, I), dtype=torch.uint8, device="cuda")
+    fns = [lambda: w4.w4a16_moe_gemm(x, idd, wts, gq, gs, dq, ds, out, ws, stream=stream)
+           for _ in range(reps + 3)]
+    t = _time_launches(stream, fns)[3:]
+    us = 1e3 * statistics.mean(t)
+    mb = active * BYTES_PER_WEIGHT * (K * 2 * I + I * K)
+    res["moe_T64_E384_top8"] = {"us": us, "active_experts": active, "algorithmic_bytes": mb,
+                                "GB/s": mb / (us * 1e-6) / 1e9,
+                                "frac_of_hbm": mb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                                "launches_per_call": 4}
+    del gq, gs, dq, ds, ws
+
+    # large-M bf16 contraction (tensor cores)
+    c = synth.PREFILL
+    M, K, N = c["M"], c["K"], c["N"]
+    try:
+        W = synth.cuda_weights(K, N, seed=3000)
+        qw, sc = w4.w4a16_quantize(W)
+        del W
+        xb = synth.cuda_bf16_activations(M, K, seed=3)
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        fns = [lambda: w4.w4a16_gemm_bf16(xb, qw, sc, yb, stream=stream) for _ in range(reps + 3)]
+        t = _time_launches(stream, fns)[3:]
+        us = 1e3 * statistics.mean(t)
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        res["prefill_M4096_K7168_N18432"] = {"us": us, "TFLOP/s": tf,
+                                             "frac_of_bf16": tf / peaks["bf16_tflops"]}
+    except Exception as ex:  # the bf16 kernel may be unavailable in this build
+        res["prefill_M4096_K7168_N18432"] = {"unavailable": str(ex).splitlines()[0]}
+
+    # tiny: launch-latency bound
+    c = synth.TINY
+    W = synth.cuda_weights(c["K"], c["N"], seed=4000)
+    qw, sc = w4.w4a16_quantize(W)
+    x = synth.cuda_normal((1, c["K"]), 1.0, seed=4, stream=1)
+    y = torch.empty((1, c["N"]), dtype=torch.float32, device="cuda")
+    fns = [lambda: w4.w4a16_gemm(x, qw, sc, y, stream=stream) for _ in range(reps + 3)]
+    t = _time_launches(stream, fns)[3:]
+    res["tiny_M1_K256_N512"] = {"us": 1e3 * statistics.mean(t)}
+    return res
+
+
+# ----------------------------------------------------------------------------- oracle (CPU)
+
+def _blas_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        n = [d.get("num_threads", 1) for d in threadpool_info() if d.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:
+        pass
+    return os.cpu_count() or 1
+
+
+class OracleWorkload:
+    """The CPU oracle (dequantize + float64 matmul + SwiGLU) on the headline workload restricted
+    to `cols` gate/up output pairs, for M = 1, 4, 16. Quantization is the offline step and is
+    done once, untimed."""
+
+    def __init__(self, cols: int):
+        import oracle
+        import synth
+        self.oracle = oracle
+        self.K, self.I = synth.SWIGLU["K"], synth.SWIGLU["I"]
+        self.cols = cols
+        W = synth.weights(self.K, 2 * cols, seed=1)   # `cols` gate + `cols` up columns
+        self.qw, self.sc = oracle.quantize_w4a16(W)
+        self.xs = {M: synth.activations(M, self.K, seed=M) for M in M_LIST}
+        self.bytes_per_step = len(M_LIST) * BYTES_PER_WEIGHT * self.K * 2 * cols
+
+    def step(self):
+        for M in M_LIST:
+            self.oracle.swiglu_gemm(self.xs[M], self.qw, self.sc)
+
+    def describe(self, n, t):
+        return (f"oracle swiglu_gemm (dequantize + float64 matmul + SwiGLU) on {self.cols} of "
+                f"{self.I} gate/up output pairs, M in {{1,4,16}}, K={self.K}; {n} steps in {t:.1f} s")
+
+
+def oracle_sample(seconds_target: float = 12.0, cols: int = 2048):
+    """Bounded CPU-oracle sample: returns (GB/s of weight bytes processed, description)."""
+    wl = OracleWorkload(cols)
+    wl.step()
+    n, t = 0, 0.0
+    while t < seconds_target:
+        t0 = time.perf_counter()
+        wl.step()
+        t += time.perf_counter() - t0
+        n += 1
+    return n * wl.bytes_per_step / t / 1e9, wl.describe(n, t)
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    wl = OracleWorkload(cols=512)
+    for _ in range(args.warmup):
+        wl.step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        wl.step()
+    t = time.perf_counter() - t0
+    value = args.steps * wl.bytes_per_step / t / 1e9
+    desc = wl.describe(args.steps, t)
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "M": list(M_LIST), "K": 7168, "N": 36864, "group": 32},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-breakdown", action="store_true", help="only the headline workload")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    if args.impl == "reference":
+        rank = int(os.environ.get("RANK", "0"))
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        out = run_reference(args, rank, world)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+
+    rank, world, _ = dist_setup(args.gpus)
+    out = run_ours(args, rank, world)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        gbs, desc = oracle_sample()
+        out["cpu_baseline"] = {"value": gbs, "unit": UNIT, "cores": _blas_threads(), "kind": "oracle",
+                               "sample": desc}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

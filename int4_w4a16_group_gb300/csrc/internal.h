@@ -1,0 +1,48 @@
+// Internal host-side interface between the C-ABI layer (abi.cu) and the kernel translation units.
+// Launchers assume their arguments were validated by abi.cu.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace w4a16 {
+
+constexpr int kGroup = 32;
+
+struct DeviceInfo {
+  int device;
+  int sm_count;
+  int cc_major, cc_minor;
+  size_t smem_optin;
+};
+// Properties of the current device (cached per device id).
+cudaError_t device_info(DeviceInfo* out);
+
+// Device address of the library's error word (one per device, lazily resolved).
+unsigned int* device_error_word();
+
+// ---- quant.cu
+cudaError_t launch_quantize(const float* W, int K, int N, int32_t* qw, float* sc, cudaStream_t s);
+cudaError_t launch_dequantize(const int32_t* qw, const float* sc, int K, int N, float* W,
+                              cudaStream_t s);
+
+// ---- gemv.cu : small-M weight-streaming kernels.
+// Dense: y[M, N] = x[M, K] @ W.  SwiGLU: y[M, N/2] = silu(gate) * up.  M <= 16 per call.
+cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, float* y, int M,
+                        int N, int K, bool swiglu, cudaStream_t s);
+constexpr int kGemvMaxM = 16;
+
+// ---- moe.cu
+size_t moe_workspace_size(int T, int topk, int E, int K, int I);
+cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T, int topk,
+                       int E, const int32_t* qw_gu, const float* sc_gu, const int32_t* qw_dn,
+                       const float* sc_dn, float* out, int K, int I, void* ws, size_t ws_bytes,
+                       cudaStream_t s);
+cudaError_t launch_topk_softmax(const float* logits, float* weights, int T, int topk,
+                                cudaStream_t s);
+
+// ---- prefill.cu : tcgen05 path
+cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
+                             int M, int N, int K, cudaStream_t s);
+
+}  // namespace w4a16

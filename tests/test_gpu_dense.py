@@ -1,0 +1,188 @@
+"""GPU parity of the dense path through the C ABI: quantize/pack (bit-exact), dequantize
+(bit-exact), w4a16_gemm and the fused gate/up SwiGLU GEMM (rel-L2 <= 1e-5), linear() dispatch
+and the raw-file loader. Small cases span several tiles and a ragged tail; the full-size
+workloads are checked on sampled output columns."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import FP32_TOL, assert_close_rows, dev, host, lib
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def w4():
+    return lib()
+
+
+# ----------------------------------------------------------------------------- format
+
+@pytest.mark.parametrize("K,N,outl", [(32, 4, False), (256, 512, False), (512, 1000, True),
+                                      (4096, 388, True)])
+def test_quantize_bit_exact(w4, K, N, outl):
+    W = synth.weights(K, N, seed=K + N, outliers=outl)
+    W[:32, :4] = 0.0                       # an all-zero group
+    if K > 32:
+        W[32:64, 1] *= np.float32(1e-37)   # a group whose scale and quotients are subnormal
+    qo, so = oracle.quantize_w4a16(W)
+    qw, sc = w4.w4a16_quantize(dev(W))
+    np.testing.assert_array_equal(host(qw), qo)
+    np.testing.assert_array_equal(host(sc), so)
+
+
+def test_dequantize_bit_exact_every_nibble(w4):
+    rng = np.random.default_rng(5)
+    K, N = 256, 132
+    q = rng.integers(-8, 8, size=(K, N))
+    q[:8, 0] = -8                          # nibble 0 (never produced by the quantizer)
+    qw = oracle.pack_int4(q)
+    sc = (rng.random((K // 32, N), dtype=np.float32) * 0.1).astype(np.float32)
+    sc[0, 3] = 0.0
+    Wg = host(w4.w4a16_dequantize(dev(qw), dev(sc)))
+    want = oracle.dequantize(qw, sc).astype(np.float32)   # q*s is exact in f64; one rounding
+    np.testing.assert_array_equal(Wg, want)
+
+
+# ----------------------------------------------------------------------------- GEMM
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 33])
+@pytest.mark.parametrize("K,N", [(512, 1000), (2048, 260)])
+def test_gemm_small(w4, M, K, N):
+    W = synth.weights(K, N, seed=M + K, outliers=True)
+    x = synth.activations(M, K, seed=M)
+    qo, so = oracle.quantize_w4a16(W)
+    y = w4.w4a16_gemm(dev(x), dev(qo), dev(so))
+    assert_close_rows(host(y), oracle.gemm(x, qo, so), FP32_TOL, f"gemm M={M} K={K} N={N}")
+
+
+def test_gemm_tiny_workload(w4):
+    c = synth.TINY
+    W = synth.weights(c["K"], c["N"], seed=0)
+    x = synth.activations(c["M"], c["K"], seed=0)
+    qo, so = oracle.quantize_w4a16(W)
+    qw, sc = w4.w4a16_quantize(dev(W))
+    y = w4.w4a16_gemm(dev(x), qw, sc)
+    assert_close_rows(host(y), oracle.gemm(x, qo, so), FP32_TOL, "tiny")
+
+
+def test_gemm_handmade_extremes(w4):
+    """Nibble 0 (-8) and 15 (+7) everywhere, a zero-scale group, large and tiny scales."""
+    K, N, M = 128, 64, 3
+    q = np.full((K, N), -8)
+    q[:, 1::2] = 7
+    qw = oracle.pack_int4(q)
+    sc = np.full((K // 32, N), 0.5, dtype=np.float32)
+    sc[1, :] = 0.0
+    sc[2, :8] = 1e20
+    sc[3, 8:16] = 1e-20
+    x = synth.activations(M, K, seed=3)
+    y = w4.w4a16_gemm(dev(x), dev(qw), dev(sc))
+    assert_close_rows(host(y), oracle.gemm(x, qw, sc), FP32_TOL, "extremes")
+
+
+def test_gemm_zero_weights_and_empty(w4):
+    K, N = 256, 128
+    qw, sc = oracle.quantize_w4a16(np.zeros((K, N), dtype=np.float32))
+    x = synth.activations(4, K, seed=1)
+    y = host(w4.w4a16_gemm(dev(x), dev(qw), dev(sc)))
+    assert (y == 0).all()
+    e = torch.empty((0, K), dtype=torch.float32, device="cuda")
+    assert w4.w4a16_gemm(e, dev(qw), dev(sc)).shape == (0, N)
+
+
+def test_gemm_is_deterministic(w4):
+    W = synth.weights(4096, 1024, seed=8)
+    x = synth.activations(4, 4096, seed=8)
+    qw, sc = w4.w4a16_quantize(dev(W))
+    xd = dev(x)
+    a = host(w4.w4a16_gemm(xd, qw, sc))
+    b = host(w4.w4a16_gemm(xd, qw, sc))
+    np.testing.assert_array_equal(a, b)
+
+
+# ----------------------------------------------------------------------------- SwiGLU
+
+@pytest.mark.parametrize("M", [1, 2, 4, 7, 16, 20])
+@pytest.mark.parametrize("K,I", [(1024, 520), (256, 64)])
+def test_swiglu_small(w4, M, K, I):
+    W = synth.weights(K, 2 * I, seed=M + I)
+    x = synth.activations(M, K, seed=M + 1)
+    qo, so = oracle.quantize_w4a16(W)
+    y = w4.w4a16_gemm_swiglu(dev(x), dev(qo), dev(so))
+    assert_close_rows(host(y), oracle.swiglu_gemm(x, qo, so), FP32_TOL, f"swiglu M={M}")
+
+
+# ----------------------------------------------------------------------------- full size, sampled
+
+def _sampled(w4, K, N, M, cols, outliers, x_std, seed, swiglu):
+    """Full-size weights drawn on the device, quantized by the library, GEMM at full size;
+    the oracle quantizes only the sampled weight columns (quantization is per column) and
+    computes those outputs."""
+    Wd = synth.cuda_weights(K, N, seed=seed, outliers=outliers)
+    qw, sc = w4.w4a16_quantize(Wd)
+    x = synth.activations(M, K, seed=seed + 1, std=x_std)
+    if swiglu:
+        y = w4.w4a16_gemm_swiglu(dev(x), qw, sc)
+        I = N // 2
+        wcols = np.concatenate([cols, cols + I])
+    else:
+        y = w4.w4a16_gemm(dev(x), qw, sc)
+        wcols = cols
+    idx = torch.from_numpy(wcols).cuda()
+    Wc = host(Wd.index_select(1, idx))
+    qo, so = oracle.quantize_w4a16(Wc)
+    np.testing.assert_array_equal(host(qw.index_select(1, idx)), qo)
+    np.testing.assert_array_equal(host(sc.index_select(1, idx)), so)
+    ref = oracle.swiglu_gemm(x, qo, so) if swiglu else oracle.gemm(x, qo, so)
+    got = host(y)[:, cols]
+    del Wd
+    return got, ref
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_full_size_swiglu_gate_up(w4, M):
+    K, I = synth.SWIGLU["K"], synth.SWIGLU["I"]
+    rng = np.random.default_rng(M)
+    cols = np.sort(np.concatenate([rng.choice(I, 254, replace=False), [0, I - 1]]))
+    got, ref = _sampled(w4, K, 2 * I, M, cols, False, 1.0, 100 + M, True)
+    assert_close_rows(got, ref, FP32_TOL, f"gate/up M={M}")
+
+
+@pytest.mark.parametrize("M", [1, 4, 16])
+def test_full_size_down(w4, M):
+    K, N = synth.DOWN["K"], synth.DOWN["N"]
+    rng = np.random.default_rng(M + 7)
+    cols = np.sort(np.concatenate([rng.choice(N, 254, replace=False), [0, N - 1]]))
+    got, ref = _sampled(w4, K, N, M, cols, True, synth.DOWN_X_STD, 200 + M, False)
+    assert_close_rows(got, ref, FP32_TOL, f"down M={M}")
+
+
+# ----------------------------------------------------------------------------- dispatch + loader
+
+def test_linear_dispatch_and_loader(w4, tmp_path):
+    K, N, I = 512, 256, 128
+    W = synth.weights(K, N, seed=21)
+    Wgu = synth.weights(K, 2 * I, seed=22)
+    qo, so = oracle.quantize_w4a16(W)
+    qgo, sgo = oracle.quantize_w4a16(Wgu)
+    qo.tofile(tmp_path / "down.qw")
+    so.tofile(tmp_path / "down.sc")
+    qw = torch.empty((K // 8, N), dtype=torch.int32, device="cuda")
+    sc = torch.empty((K // 32, N), dtype=torch.float32, device="cuda")
+    w4.w4a16_load_qw_sc(str(tmp_path / "down.qw"), str(tmp_path / "down.sc"), K, N, qw, sc)
+    np.testing.assert_array_equal(host(qw), qo)
+    np.testing.assert_array_equal(host(sc), so)
+    reg = w4.Registry()
+    reg.add("mlp.down", qw, sc)
+    reg.add("mlp.gate_up", dev(qgo), dev(sgo))
+    x = synth.activations(3, K, seed=23)
+    assert_close_rows(host(reg.linear("mlp.down", dev(x))), oracle.gemm(x, qo, so), FP32_TOL, "linear")
+    assert_close_rows(host(reg.linear_swiglu("mlp.gate_up", dev(x))), oracle.swiglu_gemm(x, qgo, sgo),
+                      FP32_TOL, "linear_swiglu")
+    with pytest.raises(w4.W4A16Error) as ei:
+        reg.linear("mlp.up", dev(x))
+    assert ei.value.status == 6
+    reg.close()
