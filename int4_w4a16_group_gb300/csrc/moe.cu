@@ -6,24 +6,26 @@
 // Four launches on the caller's stream:
 //   1. route    : one CTA counting-sorts the T*topk (token, slot) pairs by expert (stable, so
 //                 the order inside an expert is ascending pair index) and lists active experts;
-//   2. gate/up  : persistent CTAs over (active expert, 64+64-column tile) items; each item streams
-//                 its weight tile once for all of the expert's rows and writes silu(g)*u rows
-//                 of h[pairs, I] in expert-sorted order;
-//   3. down     : same over (active expert, 128-column tile) of the down weights, h -> y_pair;
+//   2. gate/up  : persistent CTAs over (active expert, tile of 8 slices = 128 gate + 128 up
+//                 columns) jobs; each job streams its weight tile once for all of the expert's
+//                 rows (up to 16 per pass) with the tensor-core core of mma_core.cuh and writes
+//                 silu(g)*u rows of h[pairs, I] in expert-sorted order;
+//   3. down     : same over (active expert, 256-column tile) of the down weights, h -> y_pair;
 //   4. combine  : out[t] = sum_j topk_w[t, j] * y_pair[pos(t, j)] in slot order.
 // No atomics on data, so the result is deterministic. Every weight byte of an active expert is
-// read once per call (plus re-reads for experts with more than 8 routed rows, served by L2).
+// read once per call (plus one more pass per further 16 rows for experts with more than 16).
 #include <stdint.h>
 
 #include "internal.h"
-#include "simt_core.cuh"
+#include "mma_core.cuh"
 
 namespace w4a16 {
 namespace {
 
-using namespace simt;
+using namespace mma;
 
-constexpr int kRowsPerPass = 8;  // rows of one expert processed per pass over a weight tile
+constexpr int kWN = 8;           // warps (32-column slices) per CTA
+constexpr int kRowsPerPass = 16; // rows of one expert per pass over a weight tile
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -130,50 +132,25 @@ struct GroupedArgs {
   int ldd;
 };
 
-template <int MM, bool SWIGLU>
+template <int NB, bool SWIGLU>
 __device__ __forceinline__ void grouped_pass(const GroupedArgs& a, const int32_t* qw,
-                                             const float* sc, int tile, int row0, float* red) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int col;
-  bool valid;
-  lane_columns<SWIGLU>(tile, lane, a.N, &col, &valid);
-  const float* xrow[MM];
-#pragma unroll
-  for (int m = 0; m < MM; ++m) {
+                                             const float* sc, int tile, int row0, int rows,
+                                             char* smem) {
+  const int warp = threadIdx.x >> 5;
+  auto rowptr = [&](int m) {
     const int p = row0 + m;
     const int r = a.gather ? (a.sorted_pair[p] / a.topk) : p;
-    xrow[m] = a.src + (size_t)r * a.Kr;
-  }
-  float acc[MM][4];
-#pragma unroll
-  for (int m = 0; m < MM; ++m)
-#pragma unroll
-    for (int c = 0; c < 4; ++c) acc[m][c] = 0.0f;
-  if (valid) accumulate_groups<MM>(xrow, qw, sc, a.N, col, warp, a.Kr / kGroup, kWarps, acc);
-  reduce_warps<MM>(red, acc, warp, lane);
-  if (SWIGLU) {
-    const int I = a.N >> 1;
-    for (int idx = threadIdx.x; idx < MM * 64; idx += kThreads) {
-      const int m = idx >> 6, j = idx & 63;
-      const int o = 64 * tile + j;
-      if (o < I)
-        a.dst[(size_t)(row0 + m) * a.ldd + o] =
-            silu_f(red[m * kTileN + j]) * red[m * kTileN + 64 + j];
-    }
-  } else {
-    for (int idx = threadIdx.x; idx < MM * kTileN; idx += kThreads) {
-      const int m = idx / kTileN, j = idx - m * kTileN;
-      const int o = kTileN * tile + j;
-      if (o < a.N) a.dst[(size_t)(row0 + m) * a.ldd + o] = red[m * kTileN + j];
-    }
-  }
-  __syncthreads();  // red is reused by the next pass
+    return a.src + (size_t)r * a.Kr;
+  };
+  float acc[2][NB][4];
+  stream_groups<NB, SWIGLU, kWN>(rowptr, rows, qw, sc, a.N, 0, a.Kr / kGroup, tile * kWN, smem,
+                                 acc);
+  store_direct<NB, SWIGLU>(acc, tile * kWN + warp, a.N, rows, a.dst + (size_t)row0 * a.ldd);
 }
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(kThreads) moe_grouped_kernel(GroupedArgs a) {
-  extern __shared__ float4 smem4[];
-  float* red = reinterpret_cast<float*>(smem4);  // [kWarps][kRowsPerPass][kTileN]
+__global__ void __launch_bounds__(kWN * 32, 2) moe_grouped_kernel(GroupedArgs a) {
+  extern __shared__ __align__(128) char smem[];
   const int n_active = a.hdr[0];
   const long long total = (long long)n_active * a.tiles;
   const size_t qstride = (size_t)(a.Kr / 8) * a.N;
@@ -188,15 +165,11 @@ __global__ void __launch_bounds__(kThreads) moe_grouped_kernel(GroupedArgs a) {
     const float* sc = a.sc + (size_t)e * sstride;
     for (int c0 = 0; c0 < rows; c0 += kRowsPerPass) {
       const int mr = (rows - c0) < kRowsPerPass ? (rows - c0) : kRowsPerPass;
-      switch (mr) {
-        case 1: grouped_pass<1, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        case 2: grouped_pass<2, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        case 3: grouped_pass<3, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        case 4: grouped_pass<4, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        case 5: grouped_pass<5, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        case 6: grouped_pass<6, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        case 7: grouped_pass<7, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
-        default: grouped_pass<8, SWIGLU>(a, qw, sc, tile, r0 + c0, red); break;
+      switch ((mr + 3) >> 2) {
+        case 1: grouped_pass<1, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
+        case 2: grouped_pass<2, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
+        case 3: grouped_pass<3, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
+        default: grouped_pass<4, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
       }
     }
   }
@@ -245,17 +218,20 @@ __global__ void topk_softmax_kernel(const float* __restrict__ logits, float* __r
 }
 
 template <bool SWIGLU>
-cudaError_t launch_grouped(const GroupedArgs& a, int sms, cudaStream_t s) {
-  static int occ_cache = 0;
+cudaError_t launch_grouped(const GroupedArgs& a, const DeviceInfo& di, cudaStream_t s) {
+  static int occ_cache[64] = {0};
   auto kern = moe_grouped_kernel<SWIGLU>;
-  const size_t smem = (size_t)kWarps * kRowsPerPass * kTileN * sizeof(float);
-  if (occ_cache == 0) {
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, smem);
+  constexpr int smem = Smem<4, kWN>::kBytes;
+  int& occ = occ_cache[di.device & 63];
+  if (occ == 0) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
-    occ_cache = occ < 1 ? 1 : occ;
+    int o = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kWN * 32, smem);
+    if (e != cudaSuccess) return e;
+    occ = o < 1 ? 1 : o;
   }
-  kern<<<sms * occ_cache, kThreads, smem, s>>>(a);
+  kern<<<di.sm_count * occ, kWN * 32, smem, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -301,10 +277,10 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
   gu.sc = sc_gu;
   gu.N = 2 * I;
   gu.Kr = K;
-  gu.tiles = (I + 63) / 64;
+  gu.tiles = ((I + 15) / 16 + kWN - 1) / kWN;
   gu.dst = h;
   gu.ldd = I;
-  if ((e = launch_grouped<true>(gu, di.sm_count, s)) != cudaSuccess) return e;
+  if ((e = launch_grouped<true>(gu, di, s)) != cudaSuccess) return e;
 
   GroupedArgs dn = gu;
   dn.src = h;
@@ -313,10 +289,10 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
   dn.sc = sc_dn;
   dn.N = K;
   dn.Kr = I;
-  dn.tiles = (K + kTileN - 1) / kTileN;
+  dn.tiles = ((K + 31) / 32 + kWN - 1) / kWN;
   dn.dst = ypair;
   dn.ldd = K;
-  if ((e = launch_grouped<false>(dn, di.sm_count, s)) != cudaSuccess) return e;
+  if ((e = launch_grouped<false>(dn, di, s)) != cudaSuccess) return e;
 
   const long long total4 = (long long)T * (K / 4);
   long long blocks = (total4 + 255) / 256;
