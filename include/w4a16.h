@@ -130,6 +130,29 @@ w4a16_status w4a16_moe_gemm(const float* x, const int32_t* topk_ids, const float
                             float* out, int K, int I, int group,
                             void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
+/* The same MoE block for callers that cannot allocate device memory, such as a plugin or
+ * foreign-function interface that only passes input and output buffers, or a process whose
+ * device memory another runtime has already reserved. The pages have no counterpart: this is
+ * an addition of this library.
+ *   - Arguments and results as w4a16_moe_gemm, without the workspace: the scratch is one array
+ *     of W4A16_MOE_STATIC_SCRATCH_BYTES in device memory that the library's device code holds on
+ *     every GPU that loads it, until the process exits. No allocation happens in the call.
+ *   - Sizes with w4a16_moe_workspace_size(T, topk, E, K, I) > W4A16_MOE_STATIC_SCRATCH_BYTES
+ *     are refused with W4A16_ERR_WORKSPACE before anything is launched (at K = 7168, I = 2048
+ *     that allows up to 910 token-expert pairs, e.g. T = 64 tokens with top-8).
+ *   - The first call on each device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - All calls on a device share the one array and it keeps whatever the last call left there
+ *     (nothing in it needs to start at zero). Calls whose execution overlaps on the GPU -- on
+ *     different streams, or from different host threads -- race on it; serialize them. */
+#define W4A16_MOE_STATIC_SCRATCH_BYTES (32u << 20)
+w4a16_status w4a16_moe_gemm_noalloc(const float* x, const int32_t* topk_ids,
+                                    const float* topk_w, int T, int topk, int E,
+                                    const int32_t* qw_gu, const float* sc_gu,
+                                    const int32_t* qw_dn, const float* sc_dn,
+                                    float* out, int K, int I, int group,
+                                    w4a16_stream_t stream);
+
 /* Router weights over each token's selected experts: weights[t, :] = softmax(logits[t, :]).
  * logits, weights: [T, topk] float32, 1 <= topk <= 32. */
 w4a16_status w4a16_topk_softmax(const float* logits, float* weights, int T, int topk,
