@@ -5,8 +5,8 @@
 // group-32 float32 scales); the pages measure the optimized kernel against HBM bandwidth, so the
 // design goal is to stream every packed weight and scale byte exactly once.
 //
-// Grid: x = tiles of kWN slices (32 weight columns each, one warp per slice), y = CK slices of
-// K. The CK CTAs of one tile form a thread-block cluster and add their partial tiles through
+// Grid: x = tiles of kWN slices (one warp per slice of 32 or 64 weight columns), y = CK slices
+// of K. The CK CTAs of one tile form a thread-block cluster and add their partial tiles through
 // distributed shared memory in rank order: deterministic, no global scratch, no atomics.
 // The per-warp main loop lives in mma_core.cuh.
 #include <cooperative_groups.h>
@@ -21,15 +21,26 @@ namespace {
 
 using namespace mma;
 
-constexpr int kWN = 8;  // warps (slices) per CTA
+// Warps (slices) per CTA: small CTAs for up to 8 rows (several per SM, clusters pack easily),
+// 8 warps for 9..16 rows.
+template <int NB>
+struct Warps {
+  static constexpr int value = NB <= 2 ? 4 : 8;
+};
 
-template <int NB, bool SWIGLU>
-__global__ void __launch_bounds__(kWN * 32) gemv_mma_kernel(const float* __restrict__ x,
-                                                            const int32_t* __restrict__ qw,
-                                                            const float* __restrict__ sc,
-                                                            float* __restrict__ y, int M, int N,
-                                                            int K) {
-  extern __shared__ __align__(128) char smem[];
+// Ring depth and activation budget: 2 stages and 12 KB keep a 4-warp CTA near 53 KB, so four
+// fit per SM (16 warps, ~80 KB of copies in flight); 8-warp CTAs keep 4 stages.
+template <int NB, int CH>
+using DenseGeo = Geo<NB, CH, Warps<NB>::value, NB <= 2 ? 2 : 4, NB <= 2 ? 12288 : 24576>;
+
+template <int NB, int CH, bool SWIGLU>
+__global__ void __launch_bounds__(Warps<NB>::value * 32, NB <= 2 ? 4 : 2)
+    gemv_mma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
+                    const float* __restrict__ x, float* __restrict__ y, int M, int N, int K,
+                    unsigned int* err) {
+  constexpr int kWN = Warps<NB>::value;
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = align1024(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
   const int tile = blockIdx.x;
   const int CK = (int)cluster.dim_blocks().y;
@@ -39,42 +50,48 @@ __global__ void __launch_bounds__(kWN * 32) gemv_mma_kernel(const float* __restr
   const int q0 = (int)((long long)rank * G / CK);
   const int q1 = (int)((long long)(rank + 1) * G / CK);
 
-  float acc[2][NB][4];
+  using L = DenseGeo<NB, CH>;
+  init_barriers<L>(smem, kWN);
+  float acc[CH][2][NB][4];
+  int seq = 0;
   auto rowptr = [&](int m) { return x + (size_t)m * K; };
-  stream_groups<NB, SWIGLU, kWN>(rowptr, M, qw, sc, N, q0, q1 - q0, tile * kWN, smem, acc);
+  stream_groups<NB, CH, SWIGLU, kWN, L>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN,
+                                        smem, seq, err, acc);
 
   if (CK == 1) {
-    store_direct<NB, SWIGLU>(acc, tile * kWN + warp, N, M, y);
+    store_direct<NB, CH, SWIGLU>(acc, tile * kWN + warp, N, M, y);
     return;
   }
-  // Split-K: partial tile [4*NB rows][kWN*32 local columns] in shared memory (reusing the
-  // cp.async rings), then rank r finishes its share of the columns over all ranks in order.
-  constexpr int kCols = kWN * 32;
-  float* red = reinterpret_cast<float*>(smem + Smem<NB, kWN>::kPipeOff);
+  // Split-K: partial tile [4*NB rows][kCols local columns] in shared memory (reusing the
+  // code ring), then rank r finishes its share of the columns over all ranks in order.
+  // SwiGLU tiles hold the kOut gate sums first, then the kOut matching up sums.
+  constexpr int kCols = kWN * 32 * CH;
+  constexpr int kOut = kWN * 16 * CH;
+  static_assert(4 * NB * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
+                "split-K tile must fit in the code ring");
+  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
   {
     const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-    const int h = (g >> 1) + 4 * (g & 1);
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
-      *reinterpret_cast<float4*>(&red[(4 * b + t) * kCols + warp * 32 + 4 * h]) =
-          chunk_result<NB>(acc, b);
+    for (int c = 0; c < CH; ++c)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+        *reinterpret_cast<float4*>(&red[(4 * b + t) * kCols +
+                                        tile_local_col<CH, SWIGLU, kWN>(warp, c, g)]) =
+            chunk_result<NB, CH>(acc, c, b);
   }
   cluster.sync();
   if (SWIGLU) {
-    // local output o (0 .. kWN*16-1): slice o/16, gate at local column 32 (o/16) + o%16,
-    // up at 32 (o/16) + 16 + o%16 (chunks 0..3 are gate, 4..7 up).
-    constexpr int kOut = kWN * 16;
     const int I = N >> 1;
     const int per = kOut / CK;
     for (int idx = threadIdx.x; idx < M * per; idx += blockDim.x) {
       const int m = idx / per;
       const int o = rank * per + (idx - m * per);
-      const int lc = 32 * (o >> 4) + (o & 15);
       float gs = 0.0f, us = 0.0f;
       for (int q = 0; q < CK; ++q) {
         const float* r = cluster.map_shared_rank(red, q);
-        gs += r[m * kCols + lc];
-        us += r[m * kCols + lc + 16];
+        gs += r[m * kCols + o];
+        us += r[m * kCols + kOut + o];
       }
       const int out = tile * kOut + o;
       if (out < I) y[(size_t)m * I + out] = silu_f(gs) * us;
@@ -93,31 +110,40 @@ __global__ void __launch_bounds__(kWN * 32) gemv_mma_kernel(const float* __restr
   cluster.sync();  // peers may still be reading this CTA's shared memory
 }
 
+constexpr int kMaxCluster = 16;
+
 struct LaunchCache {
   int device_mask = 0;
   int occ = 0;
-  int max_clusters[9] = {0};  // index = cluster size (1, 2, 4, 8)
+  int max_clusters[kMaxCluster + 1] = {0};  // index = cluster size
 };
 
-template <int NB, bool SWIGLU>
-cudaError_t launch_nb(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
-                      int K, const DeviceInfo& di, cudaStream_t s) {
+// Slices (one warp each) of a problem for CH chunks per lane.
+template <int CH, bool SWIGLU>
+int slices_of(int N) {
+  return SWIGLU ? ((N >> 1) + 16 * CH - 1) / (16 * CH) : (N + 32 * CH - 1) / (32 * CH);
+}
+
+template <int NB, int CH, bool SWIGLU>
+cudaError_t launch_cfg(const float* x, const int32_t* qw, const float* sc, float* y, int M,
+                       int N, int K, const DeviceInfo& di, cudaStream_t s) {
+  constexpr int kWN = Warps<NB>::value;
   static LaunchCache cache;
-  auto kern = gemv_mma_kernel<NB, SWIGLU>;
-  constexpr int smem = Smem<NB, kWN>::kBytes;
-  static_assert(4 * NB * kWN * 32 * 4 <= Smem<NB, kWN>::kPipeBytes, "split-K tile must fit");
-  const int slices = SWIGLU ? ((N >> 1) + 15) / 16 : (N + 31) / 32;
-  const int tiles = (slices + kWN - 1) / kWN;
+  auto kern = gemv_mma_kernel<NB, CH, SWIGLU>;
+  constexpr int smem = DenseGeo<NB, CH>::kAlloc;
+  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
   const int G = K / kGroup;
   const int bit = 1 << (di.device & 31);
   if (!(cache.device_mask & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWN * 32, smem);
     if (e != cudaSuccess) return e;
     cache.occ = occ < 1 ? 1 : occ;
-    for (int ck = 1; ck <= 8; ck *= 2) {
+    for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1, ck, 1);
       cfg.blockDim = dim3(kWN * 32, 1, 1);
@@ -138,12 +164,13 @@ cudaError_t launch_nb(const float* x, const int32_t* qw, const float* sc, float*
     }
     cache.device_mask |= bit;
   }
-  // Pick the K split whose waves of clusters fill the GPU most evenly.
+  // Pick the K split whose waves of clusters fill the GPU most evenly; each CTA keeps at
+  // least 8 groups of K.
   const double slots = (double)di.sm_count * cache.occ;
   int CK = 1;
   double best = -1.0;
-  for (int ck = 1; ck <= 8; ck *= 2) {
-    if (ck > 1 && G / ck < 4) break;
+  for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
+    if (ck > 1 && G / ck < 8) break;
     const int nc = cache.max_clusters[ck];
     if (nc <= 0) continue;
     const long long waves = (tiles + nc - 1) / nc;
@@ -153,6 +180,11 @@ cudaError_t launch_nb(const float* x, const int32_t* qw, const float* sc, float*
       CK = ck;
     }
   }
+  CUtensorMap tq, ts;
+  cudaError_t e = make_tmap(&tq, 0, qw, (uint64_t)N, (uint64_t)(K / 8), 1, 32, kRows);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&ts, 1, sc, (uint64_t)N, (uint64_t)(K / kGroup), 1, 32, kRows / 4);
+  if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(tiles, CK, 1);
   cfg.blockDim = dim3(kWN * 32, 1, 1);
@@ -165,17 +197,24 @@ cudaError_t launch_nb(const float* x, const int32_t* qw, const float* sc, float*
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, x, qw, sc, y, M, N, K);
+  return cudaLaunchKernelEx(&cfg, kern, tq, ts, x, y, M, N, K, device_error_word());
 }
 
+// Up to 4 rows: 4 tiles per warp (128 columns) when the problem is wide enough to give every
+// SM several warps, else 2; 5..8 rows: 2; 9..16 rows: 1 (2 with the fused SwiGLU, which pairs
+// gate and up tiles), for the register budget.
 template <bool SWIGLU>
 cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
                      int K, const DeviceInfo& di, cudaStream_t s) {
+  const bool wide = slices_of<4, SWIGLU>(N) * 8 >= 2 * di.sm_count;
+  constexpr int CH_BIG = SWIGLU ? 2 : 1;
   switch ((M + 3) / 4) {
-    case 1: return launch_nb<1, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    case 2: return launch_nb<2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    case 3: return launch_nb<3, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    case 4: return launch_nb<4, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+    case 1:
+      return wide ? launch_cfg<1, 4, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
+                  : launch_cfg<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+    case 2: return launch_cfg<2, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+    case 3: return launch_cfg<3, CH_BIG, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+    case 4: return launch_cfg<4, CH_BIG, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -1,6 +1,7 @@
 // Internal host-side interface between the C-ABI layer (abi.cu) and the kernel translation units.
 // Launchers assume their arguments were validated by abi.cu.
 #pragma once
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -20,6 +21,11 @@ cudaError_t device_info(DeviceInfo* out);
 
 // Device address of the library's error word (one per device, lazily resolved).
 unsigned int* device_error_word();
+
+// ---- tmap.cu : TMA descriptor of a row-major [d2][d1][d0] tensor of 4-byte elements, box
+// (b0 x b1 x 1); kind 0 = packed codes (int32, 128-byte swizzle), 1 = scales (float32).
+cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint32_t b0, uint32_t b1);
 
 // ---- quant.cu
 cudaError_t launch_quantize(const float* W, int K, int N, int32_t* qw, float* sc, cudaStream_t s);

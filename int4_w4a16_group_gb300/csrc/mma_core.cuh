@@ -1,12 +1,14 @@
 // Tensor-core weight-streaming core for small M (decode / draft-tree verify).
 //
-// Each warp owns a slice of 32 weight columns and walks the CTA's K range one group (32 k) at a
-// time. Per group it:
-//   * receives, through a private cp.async ring in shared memory, one 16-byte chunk per lane of
-//     the packed weights (4 consecutive columns of one packed row) and the group's scales;
-//   * turns the 4 words into fp16 MMA A-fragments with two bit tricks: (w & 0x000F000F) |
-//     0x64006400 is the fp16 pair (1024 + nibble_0, 1024 + nibble_4), and the same mask
-//     shifted by 4 gives 1024 + 16 * nibble; one fp16 FMA then yields nibble - 8 exactly;
+// Each warp owns a slice of 32*CH weight columns and walks the CTA's K range two groups
+// (2 x 32 k) per pipeline stage. Per stage it:
+//   * receives, by TMA (one elected lane issues 2*CH tile copies into a 4-stage ring with an
+//     mbarrier per stage), CH tiles of 32 columns x 8 packed rows of the codes (128-byte
+//     swizzle, so the lanes' 16-byte reads below are bank-conflict free) and CH tiles of
+//     32 columns x 2 rows of the scales;
+//   * turns each lane's 4 words per tile into fp16 MMA A-fragments with two bit tricks:
+//     (w & 0x000F000F) | 0x64006400 is the fp16 pair (1024 + nibble_0, 1024 + nibble_4), and the
+//     same mask shifted by 4 gives 1024 + 16 * nibble; one fp16 FMA then yields nibble - 8;
 //   * multiplies them with the activations on the tensor cores (mma.sync m16n8k16, fp16 in,
 //     fp32 accumulate) -- the activations enter as two fp16 terms, x * 2^-e = hi + lo with a
 //     per-group power-of-two e, which carries 22 significant bits of each float32 activation;
@@ -25,11 +27,12 @@
 //     pre-permuted as (0, 4, 1, 5, 2, 6, 3, 7) so that one 16-byte shared load gives b0/b1 of
 //     both k-steps.
 //   C (16 x 8): lane (g, t) ends with row m = 4b + t, terms hi/lo, for its two A rows.
-// Chunk mapping: lane (g, t) loads columns 4 h(g) .. 4 h(g) + 3 of its slice with
-//   h(g) = g / 2 + 4 (g % 2); A tile T (0, 1) uses columns 4 h + 2T (row g) and 4 h + 2T + 1
-//   (row g + 8). For the fused SwiGLU slice (16 gate + 16 up columns) even g hold gate
-//   columns and odd g the matching up columns, one lane apart by xor 4.
+// Chunk mapping: in each 32-column tile lane (g, t) owns the 16-byte chunk h(g) = g/2 + 4 (g%2),
+//   i.e. columns 4 h .. 4 h + 3; A tile T (0, 1) uses columns 4h + 2T (row g) and 4h + 2T + 1
+//   (row g + 8). With the 128-byte swizzle (16-byte chunk index XOR row % 8) the 8 lanes of
+//   each quarter-warp then hit 8 different bank groups.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
@@ -37,34 +40,87 @@
 namespace w4a16 {
 namespace mma {
 
-constexpr int kStages = 8;           // cp.async ring depth per warp
-constexpr int kStageBytes = 640;     // 512 B of packed words + 128 B of scales
-constexpr int kXChunkBytes = 512;    // per (group, n8 block): 32 lanes x 16 B
+constexpr int kXChunkBytes = 512;  // activation fragments per (group, n8 block): 32 lanes x 16 B
+
+// ------------------------------------------------------------------------------ PTX helpers
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, int src_bytes) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-               "r"(src_bytes)
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ float lds32f(uint32_t addr) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];\n" : "=f"(v) : "r"(addr));
+  return v;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+  return t;
+}
+// Waits for phase `parity` of the barrier; gives up after `limit_ns` and returns false.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
+// TMA tile copy of a 3-D tensor into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                         uint32_t b1) {
-  asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// Tensor-core product with a zero accumulator input (no register moves to clear d).
+__device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                           uint32_t b1, float zero) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%10,%10,%10};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(zero));
 }
 
 // (a & mask) | 0x64006400 in one LOP3.
@@ -101,6 +157,8 @@ __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
 
 // Exact power of two 2^e for e in [-126, 127].
 __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) << 23); }
+
+// ------------------------------------------------------------------------------ activations
 
 // One warp prepares the B fragments of one group q (inputs 32q .. 32q + 31) for rows
 // 0 .. M-1 (rows >= M are zero): writes NB x 512 B at dst and the group's 2^e at *fscale.
@@ -154,191 +212,309 @@ __device__ __forceinline__ void prep_group(const RowPtr& rowptr, int M, int q, c
   if (lane == 0) *fscale = exp2i(ex - 14);
 }
 
-// Shared-memory layout of one CTA of WN warps with NB n8-blocks:
-//   [x fragments: 2 buffers x WN groups x NB x 512 B][2^e per group: 2 x WN floats, padded]
-//   [cp.async rings: WN warps x kStages x 640 B]
-template <int NB, int WN>
-struct Smem {
-  static constexpr int kXBytes = 2 * WN * NB * kXChunkBytes;
-  static constexpr int kFBytes = ((2 * WN * 4) + 127) / 128 * 128;
-  static constexpr int kPipeOff = kXBytes + kFBytes;
-  static constexpr int kPipeBytes = WN * kStages * kStageBytes;
-  static constexpr int kBytes = kPipeOff + kPipeBytes;
+// ------------------------------------------------------------------------------ geometry
+
+constexpr int kRows = 8;     // packed rows per stage (2 groups)
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // give up a barrier wait after 2 s
+
+// Shared-memory layout of one CTA (offsets from a 1024-byte aligned base). Everything up to
+// the x region depends only on CH and WN, so kernels that switch NB per job share barriers:
+//   codes   WN x R x CH tiles of 8 x 128 B (swizzled)
+//   scales  WN x R x CH tiles of 2 x 128 B
+//   bars    WN x R mbarriers (padded to 128 B)
+//   x       activation fragments: the CTA's whole K range when it fits in XB bytes, else two
+//           alternating halves
+//   fscale  2^e per prepared group
+// R = stages per warp ring, XB = activation-fragment budget.
+template <int NB, int CH, int WN, int R, int XB>
+struct Geo {
+  static constexpr int kRing = R;
+  static constexpr int kCodeTile = kRows * 128;
+  static constexpr int kScaleTile = (kRows / 4) * 128;
+  static constexpr int kCodeOff = 0;
+  static constexpr int kScaleOff = kCodeOff + WN * kRing * CH * kCodeTile;
+  static constexpr int kBarOff = kScaleOff + WN * kRing * CH * kScaleTile;
+  static constexpr int kXOff = kBarOff + ((WN * kRing * 8 + 127) / 128) * 128;
+  static constexpr int kXGroups = (XB / (NB * kXChunkBytes)) & ~1;
+  static constexpr int kFOff = kXOff + kXGroups * NB * kXChunkBytes;
+  static constexpr int kBytes = kFOff + ((kXGroups * 4 + 127) / 128) * 128;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base
+  static constexpr uint32_t kStageTx = CH * (kCodeTile + kScaleTile);
 };
 
-// Column of the 4-column chunk lane (g, t) streams in slice `slice`, and whether it exists.
-// Plain: the slice is columns 32 slice .. +31.  SwiGLU (N = 2I): the slice is gate columns
-// 16 slice .. +15 and up columns I + 16 slice .. +15; even g hold gate, odd g the matching up.
-template <bool SWIGLU>
-__device__ __forceinline__ void chunk_column(int slice, int g, int N, int* col, bool* valid) {
-  if (SWIGLU) {
-    const int I = N >> 1;
-    const int j = 16 * slice + 4 * (g >> 1);
-    *valid = j < I;
-    *col = (g & 1) ? I + j : j;
-  } else {
-    const int h = (g >> 1) + 4 * (g & 1);
-    *col = 32 * slice + 4 * h;
-    *valid = *col < N;
-  }
+// First 1024-byte aligned address (in the shared window) at or after p.
+__device__ __forceinline__ char* align1024(char* p) {
+  const uint32_t s = smem_u32(p);
+  return p + ((1024u - (s & 1023u)) & 1023u);
 }
 
-// The CTA's warps stream groups q0 .. q0 + nq - 1 of their slices (slice = slice0 + warp) and
-// accumulate, per lane, acc[T][b][r] (A tile T, n8 block b, C register r).
-// rowptr(m) -> pointer to row m (< M) of the float32 activations (K floats).
-// All threads of the CTA must call this (it synchronizes the CTA between x chunks).
-template <int NB, bool SWIGLU, int WN, typename RowPtr>
-__device__ __forceinline__ void stream_groups(const RowPtr& rowptr, int M, const int32_t* qw,
-                                              const float* sc, int N, int q0, int nq,
-                                              int slice0, char* smem, float (&acc)[2][NB][4]) {
-  using L = Smem<NB, WN>;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  char* xbuf = smem;
-  float* fsc = reinterpret_cast<float*>(smem + L::kXBytes);
-  char* ring = smem + L::kPipeOff + warp * kStages * kStageBytes;
-  const uint32_t ring_s = smem_u32(ring);
+__device__ __forceinline__ int lane_chunk(int g) { return (g >> 1) + 4 * (g & 1); }
 
-  int col;
-  bool valid;
-  chunk_column<SWIGLU>(slice0 + warp, g, N, &col, &valid);
-  const bool warp_active = __any_sync(0xffffffffu, valid);
-  const int nbytes = valid ? 16 : 0;
-  const int32_t* qsrc = valid ? qw + col : qw;
-  const float* ssrc = valid ? sc + col : sc;
-
-#pragma unroll
-  for (int T = 0; T < 2; ++T)
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) acc[T][b][r] = 0.0f;
-
-  auto issue = [&](int s) {
-    const int q = q0 + s;
-    const uint32_t st = ring_s + (s % kStages) * kStageBytes;
-    cp_async16(st + lane * 16, qsrc + (size_t)(4 * q + t) * N, nbytes);
-    if (t == 0) cp_async16(st + 512 + g * 16, ssrc + (size_t)q * N, nbytes);
-  };
-
-  if (warp_active) {
-#pragma unroll
-    for (int s = 0; s < kStages - 1; ++s) {
-      if (s < nq) issue(s);
-      cp_async_commit();
-    }
+// Tensor column of the 32-column tile c of slice s.
+//   plain         : 32 CH s + 32 c.
+//   SwiGLU (CH>=2): tiles c < CH/2 are gate columns 16 CH s + 32 c; tiles c >= CH/2 the
+//                   matching up columns I + 16 CH s + 32 (c - CH/2).
+template <int CH, bool SWIGLU>
+__device__ __forceinline__ int tile_x(int slice, int c, int N) {
+  if (SWIGLU) {
+    constexpr int H = CH / 2;
+    const int j = 32 * H * slice + 32 * (c >= H ? c - H : c);
+    return c >= H ? (N >> 1) + j : j;
   }
-  if (warp < nq) prep_group<NB>(rowptr, M, q0 + warp, xbuf + warp * NB * kXChunkBytes, &fsc[warp]);
+  return 32 * CH * slice + 32 * c;
+}
+
+// Output position of the lane's 4 columns of tile c: plain -> weight column (valid if < N);
+// SwiGLU -> output index j of gate tile c (valid if < I).
+template <int CH, bool SWIGLU>
+__device__ __forceinline__ int out_col(int slice, int c, int g, int N, bool* valid) {
+  if (SWIGLU) {
+    constexpr int H = CH / 2;
+    const int j = 32 * H * slice + 32 * c + 4 * lane_chunk(g);
+    *valid = j < (N >> 1);
+    return j;
+  }
+  const int col = 32 * CH * slice + 32 * c + 4 * lane_chunk(g);
+  *valid = col < N;
+  return col;
+}
+
+// ------------------------------------------------------------------------------ main loop
+
+// Initializes this warp's stage barriers (once per kernel, before the first stream_groups).
+template <typename L>
+__device__ __forceinline__ void init_barriers(char* base, int warps) {
+  constexpr int kRing = L::kRing;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  (void)warps;
+  if (lane == 0) {
+    const uint32_t bar_s = smem_u32(base + L::kBarOff) + warp * kRing * 8;
+    for (int i = 0; i < kRing; ++i) mbar_init(bar_s + i * 8, 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+}
+
+// The CTA's warps stream groups q0 .. q0 + nq - 1 of their slices (slice = slice0 + warp) of
+// matrix `z` of the descriptors, accumulating acc[c][T][b][r] (tile c, A tile T, n8 block b,
+// C register r). `seq` counts the stages this warp has used so far (barrier phases carry on
+// across calls). Returns false if a barrier wait gave up (the error word is then set).
+// All threads of the CTA must call this (it synchronizes the CTA around the x fragments).
+template <int NB, int CH, bool SWIGLU, int WN, typename L, typename RowPtr>
+__device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
+                                              const CUtensorMap* tq, const CUtensorMap* ts,
+                                              int z, int N, int q0, int nq, int slice0,
+                                              char* base, int& seq, unsigned int* err,
+                                              float (&acc)[CH][2][NB][4]) {
+  static_assert(!SWIGLU || CH >= 2, "fused SwiGLU tiles pair gate and up tiles");
+  constexpr int kRing = L::kRing;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int slice = slice0 + warp;
+  const uint32_t code_s = smem_u32(base + L::kCodeOff) + warp * kRing * CH * L::kCodeTile;
+  const uint32_t scale_s = smem_u32(base + L::kScaleOff) + warp * kRing * CH * L::kScaleTile;
+  const uint32_t bar_s = smem_u32(base + L::kBarOff) + warp * kRing * 8;
+  char* xbuf = base + L::kXOff;
+  float* fsc = reinterpret_cast<float*>(base + L::kFOff);
+
+  // Is any column of this warp's slice inside the matrix? (Its first columns are.)
+  bool any;
+  out_col<CH, SWIGLU>(slice, 0, 0, N, &any);
+
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+#pragma unroll
+    for (int T = 0; T < 2; ++T)
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc[c][T][b][r] = 0.0f;
+
+  const int nst = (nq + 1) >> 1;  // stages of 2 groups (the last may hold 1)
+  auto issue = [&](int s) {       // lane 0 only
+    const int u = seq + s;
+    const int st = u % kRing;
+    const uint32_t bar = bar_s + st * 8;
+    mbar_expect_tx(bar, L::kStageTx);
+    const int row = 4 * (q0 + 2 * s);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int x = tile_x<CH, SWIGLU>(slice, c, N);
+      tma_load_3d(code_s + (st * CH + c) * L::kCodeTile, tq, x, row, z, bar);
+      tma_load_3d(scale_s + (st * CH + c) * L::kScaleTile, ts, x, q0 + 2 * s, z, bar);
+    }
+  };
+  if (any && lane == 0) {
+    for (int s = 0; s < kRing - 1 && s < nst; ++s) issue(s);
+  }
+
+  // Activation fragments: everything at once when it fits, else alternating halves.
+  const int pg = nq <= L::kXGroups ? ((nq + 1) & ~1) : L::kXGroups / 2;
+  auto prep_chunk = [&](int pc, int buf) {
+    for (int j = warp; j < pg; j += WN) {
+      const int qi = pc * pg + j;
+      if (qi < nq)
+        prep_group<NB>(rowptr, M, q0 + qi, xbuf + (buf * pg + j) * NB * kXChunkBytes,
+                       &fsc[buf * pg + j]);
+    }
+  };
+  prep_chunk(0, 0);
   __syncthreads();
 
-  const int nchunks = (nq + WN - 1) / WN;
-  for (int c = 0; c < nchunks; ++c) {
-    const int buf = c & 1;
-    const int qn = (c + 1) * WN + warp;
-    if (qn < nq)
-      prep_group<NB>(rowptr, M, q0 + qn, xbuf + ((buf ^ 1) * WN + warp) * NB * kXChunkBytes,
-                     &fsc[(buf ^ 1) * WN + warp]);
-    const int iend = (nq - c * WN) < WN ? (nq - c * WN) : WN;
-    if (warp_active) {
-      for (int i = 0; i < iend; ++i) {
-        const int s = c * WN + i;
-        if (s + kStages - 1 < nq) issue(s + kStages - 1);
-        cp_async_commit();
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
-        const char* st = ring + (s % kStages) * kStageBytes;
-        const uint4 wq = *reinterpret_cast<const uint4*>(st + lane * 16);
-        const float4 s4 = *reinterpret_cast<const float4*>(st + 512 + g * 16);
-        const float fg = fsc[buf * WN + i];
-        const char* xb = xbuf + (buf * WN + i) * NB * kXChunkBytes + lane * 16;
-        uint4 bf[NB];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) bf[b] = *reinterpret_cast<const uint4*>(xb + b * kXChunkBytes);
-        __syncwarp();  // the stage may be refilled by the next issue
-        uint32_t p[4][4];
-        unpack_word(wq.x, p[0]);
-        unpack_word(wq.y, p[1]);
-        unpack_word(wq.z, p[2]);
-        unpack_word(wq.w, p[3]);
-        float d[2][NB][4];
-#pragma unroll
-        for (int T = 0; T < 2; ++T)
-#pragma unroll
-          for (int b = 0; b < NB; ++b)
-#pragma unroll
-            for (int r = 0; r < 4; ++r) d[T][b][r] = 0.0f;
-#pragma unroll
-        for (int T = 0; T < 2; ++T) {
-          const uint32_t a0[4] = {p[2 * T][0], p[2 * T + 1][0], p[2 * T][1], p[2 * T + 1][1]};
-          const uint32_t a1[4] = {p[2 * T][2], p[2 * T + 1][2], p[2 * T][3], p[2 * T + 1][3]};
-#pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            mma_f16(d[T][b], a0, bf[b].x, bf[b].y);
-            mma_f16(d[T][b], a1, bf[b].z, bf[b].w);
+  bool ok = true;
+  int fail_s = 0;
+  const float zero = 0.0f;
+  const uint32_t xbuf_s = smem_u32(xbuf) + lane * 16;
+  const uint32_t fsc_s = smem_u32(fsc);
+  const int h = lane_chunk(g);
+  const int nchunks = (nq + pg - 1) / pg;
+  const int sps = pg >> 1;  // stages per x chunk
+  for (int pc = 0; pc < nchunks; ++pc) {
+    const int buf = pc & 1;
+    if (pc + 1 < nchunks) prep_chunk(pc + 1, buf ^ 1);
+    const int s_end = ((pc + 1) * sps < nst) ? (pc + 1) * sps : nst;
+    if (any) {
+      for (int s = pc * sps; s < s_end; ++s) {
+        if (ok && lane == 0 && s + kRing - 1 < nst) issue(s + kRing - 1);
+        const int u = seq + s;
+        const int st = u % kRing;
+        if (ok) {
+          const bool got = mbar_wait(bar_s + st * 8, (u / kRing) & 1, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, got)) {  // warp-uniform decision
+            ok = false;
+            fail_s = s;
+            if (lane == 0 && err) atomicCAS(err, 0u, 8u);  // W4A16_ERR_TIMEOUT
           }
         }
-        const float sv[4] = {s4.x * fg, s4.y * fg, s4.z * fg, s4.w * fg};
+        if (ok) {
 #pragma unroll
-        for (int T = 0; T < 2; ++T)
+          for (int j = 0; j < 2; ++j) {
+            const int qi = 2 * s + j;
+            if (qi < nq) {
+              const int r = 4 * j + t;
+              const uint32_t coff = r * 128 + ((h ^ (r & 7)) << 4);
+              uint4 wq[CH];
+              float4 s4[CH];
 #pragma unroll
-          for (int b = 0; b < NB; ++b) {
-            acc[T][b][0] = fmaf(sv[2 * T], d[T][b][0], acc[T][b][0]);
-            acc[T][b][1] = fmaf(sv[2 * T], d[T][b][1], acc[T][b][1]);
-            acc[T][b][2] = fmaf(sv[2 * T + 1], d[T][b][2], acc[T][b][2]);
-            acc[T][b][3] = fmaf(sv[2 * T + 1], d[T][b][3], acc[T][b][3]);
+              for (int c = 0; c < CH; ++c) {
+                wq[c] = lds128(code_s + (st * CH + c) * L::kCodeTile + coff);
+                const uint4 u4 =
+                    lds128(scale_s + (st * CH + c) * L::kScaleTile + j * 128 + h * 16);
+                s4[c] = make_float4(__uint_as_float(u4.x), __uint_as_float(u4.y),
+                                    __uint_as_float(u4.z), __uint_as_float(u4.w));
+              }
+              const int xi = buf * pg + (qi - pc * pg);
+              const float fg = lds32f(fsc_s + xi * 4);
+              uint4 bf[NB];
+#pragma unroll
+              for (int b = 0; b < NB; ++b) bf[b] = lds128(xbuf_s + (xi * NB + b) * kXChunkBytes);
+#pragma unroll
+              for (int c = 0; c < CH; ++c) {
+                uint32_t p[4][4];
+                unpack_word(wq[c].x, p[0]);
+                unpack_word(wq[c].y, p[1]);
+                unpack_word(wq[c].z, p[2]);
+                unpack_word(wq[c].w, p[3]);
+                const float sv[4] = {s4[c].x * fg, s4[c].y * fg, s4[c].z * fg, s4[c].w * fg};
+#pragma unroll
+                for (int T = 0; T < 2; ++T) {
+                  const uint32_t a0[4] = {p[2 * T][0], p[2 * T + 1][0], p[2 * T][1],
+                                          p[2 * T + 1][1]};
+                  const uint32_t a1[4] = {p[2 * T][2], p[2 * T + 1][2], p[2 * T][3],
+                                          p[2 * T + 1][3]};
+#pragma unroll
+                  for (int b = 0; b < NB; ++b) {
+                    float d[4];
+                    mma_f16_zc(d, a0, bf[b].x, bf[b].y, zero);
+                    mma_f16(d, a1, bf[b].z, bf[b].w);
+                    acc[c][T][b][0] = fmaf(sv[2 * T], d[0], acc[c][T][b][0]);
+                    acc[c][T][b][1] = fmaf(sv[2 * T], d[1], acc[c][T][b][1]);
+                    acc[c][T][b][2] = fmaf(sv[2 * T + 1], d[2], acc[c][T][b][2]);
+                    acc[c][T][b][3] = fmaf(sv[2 * T + 1], d[3], acc[c][T][b][3]);
+                  }
+                }
+              }
+            }
           }
+        }
+        __syncwarp();  // every lane is done with stage st before lane 0 refills it
       }
     }
-    __syncthreads();
+    if (nchunks > 1) __syncthreads();
   }
-  cp_async_wait<0>();
-  __syncthreads();  // the ring area may be reused by the caller's epilogue
+  if (any && !ok) {
+    // Let the copies still in flight (stages fail_s .. fail_s + kRing - 2 at most) land before
+    // the shared memory is reused or released.
+    for (int s = fail_s; s < nst && s < fail_s + kRing; ++s) {
+      const int u = seq + s;
+      (void)mbar_wait(bar_s + (u % kRing) * 8, (u / kRing) & 1, kWaitLimitNs / 16);
+    }
+  }
+  if (any) seq += nst;  // barrier phases advance only for warps that used them
+  __syncthreads();  // the caller may reuse the code ring for its epilogue
+  return ok;
 }
 
-// Per lane: the 4 finished outputs (hi + lo terms) of row m = 4b + t for the lane's chunk.
-template <int NB>
-__device__ __forceinline__ float4 chunk_result(const float (&acc)[2][NB][4], int b) {
-  return make_float4(acc[0][b][0] + acc[0][b][1], acc[0][b][2] + acc[0][b][3],
-                     acc[1][b][0] + acc[1][b][1], acc[1][b][2] + acc[1][b][3]);
+// ------------------------------------------------------------------------------ epilogues
+
+// Per lane: the 4 finished outputs (hi + lo terms) of row m = 4b + t for tile c.
+template <int NB, int CH>
+__device__ __forceinline__ float4 chunk_result(const float (&acc)[CH][2][NB][4], int c, int b) {
+  return make_float4(acc[c][0][b][0] + acc[c][0][b][1], acc[c][0][b][2] + acc[c][0][b][3],
+                     acc[c][1][b][0] + acc[c][1][b][1], acc[c][1][b][2] + acc[c][1][b][3]);
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-__device__ __forceinline__ float4 shfl_xor4(float4 v, int m) {
-  v.x = __shfl_xor_sync(0xffffffffu, v.x, m);
-  v.y = __shfl_xor_sync(0xffffffffu, v.y, m);
-  v.z = __shfl_xor_sync(0xffffffffu, v.z, m);
-  v.w = __shfl_xor_sync(0xffffffffu, v.w, m);
-  return v;
+__device__ __forceinline__ float4 swiglu4(float4 gt, float4 up) {
+  return make_float4(silu_f(gt.x) * up.x, silu_f(gt.y) * up.y, silu_f(gt.z) * up.z,
+                     silu_f(gt.w) * up.w);
 }
 
 // Writes the lane's finished outputs straight to y (used when one CTA covers the whole K).
-// Plain: y[M, N].  SwiGLU: y[M, N/2] = silu(gate) * up, combined across lane pairs (xor 4).
-template <int NB, bool SWIGLU>
-__device__ __forceinline__ void store_direct(const float (&acc)[2][NB][4], int slice, int N,
+// Plain: y[M, N].  SwiGLU: y[M, N/2] = silu(gate) * up (gate tile c pairs with up tile c+CH/2).
+template <int NB, int CH, bool SWIGLU>
+__device__ __forceinline__ void store_direct(const float (&acc)[CH][2][NB][4], int slice, int N,
                                              int M, float* y) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  int col;
-  bool valid;
-  chunk_column<SWIGLU>(slice, g, N, &col, &valid);
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const int m = 4 * b + t;
-    float4 v = chunk_result<NB>(acc, b);
+    if (m >= M) continue;
     if (SWIGLU) {
-      const float4 u = shfl_xor4(v, 4);
+      constexpr int H = CH / 2;
       const int I = N >> 1;
-      if (!(g & 1) && valid && m < M) {
-        float4 o;
-        o.x = silu_f(v.x) * u.x;
-        o.y = silu_f(v.y) * u.y;
-        o.z = silu_f(v.z) * u.z;
-        o.w = silu_f(v.w) * u.w;
-        *reinterpret_cast<float4*>(y + (size_t)m * I + col) = o;
+#pragma unroll
+      for (int c = 0; c < H; ++c) {
+        bool valid;
+        const int j = out_col<CH, SWIGLU>(slice, c, g, N, &valid);
+        if (valid)
+          *reinterpret_cast<float4*>(y + (size_t)m * I + j) =
+              swiglu4(chunk_result<NB, CH>(acc, c, b), chunk_result<NB, CH>(acc, c + H, b));
       }
-    } else if (valid && m < M) {
-      *reinterpret_cast<float4*>(y + (size_t)m * N + col) = v;
+    } else {
+#pragma unroll
+      for (int c = 0; c < CH; ++c) {
+        bool valid;
+        const int col = out_col<CH, SWIGLU>(slice, c, g, N, &valid);
+        if (valid)
+          *reinterpret_cast<float4*>(y + (size_t)m * N + col) = chunk_result<NB, CH>(acc, c, b);
+      }
     }
   }
+}
+
+// Tile-local column of tile c of lane g in a split-K reduction tile (plain: weight column
+// within the CTA tile; SwiGLU: gate output index within the tile, with the up values stored
+// WN*16*CH columns later).
+template <int CH, bool SWIGLU, int WN>
+__device__ __forceinline__ int tile_local_col(int warp, int c, int g) {
+  const int h4 = 4 * lane_chunk(g);
+  if (SWIGLU) {
+    constexpr int H = CH / 2;
+    constexpr int SO = 16 * CH;  // outputs per slice
+    return (c >= H ? WN * SO : 0) + warp * SO + 32 * (c >= H ? c - H : c) + h4;
+  }
+  return warp * 32 * CH + 32 * c + h4;
 }
 
 }  // namespace mma

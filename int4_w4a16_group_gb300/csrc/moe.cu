@@ -6,14 +6,14 @@
 // Four launches on the caller's stream:
 //   1. route    : one CTA counting-sorts the T*topk (token, slot) pairs by expert (stable, so
 //                 the order inside an expert is ascending pair index) and lists active experts;
-//   2. gate/up  : persistent CTAs over (active expert, tile of 8 slices = 128 gate + 128 up
+//   2. gate/up  : persistent CTAs over (active expert, tile of 8 slices = 256 gate + 256 up
 //                 columns) jobs; each job streams its weight tile once for all of the expert's
-//                 rows (up to 16 per pass) with the tensor-core core of mma_core.cuh and writes
+//                 rows (up to 8 per pass) with the tensor-core core of mma_core.cuh and writes
 //                 silu(g)*u rows of h[pairs, I] in expert-sorted order;
-//   3. down     : same over (active expert, 256-column tile) of the down weights, h -> y_pair;
+//   3. down     : same over (active expert, 512-column tile) of the down weights, h -> y_pair;
 //   4. combine  : out[t] = sum_j topk_w[t, j] * y_pair[pos(t, j)] in slot order.
 // No atomics on data, so the result is deterministic. Every weight byte of an active expert is
-// read once per call (plus one more pass per further 16 rows for experts with more than 16).
+// read once per call (plus one more pass per further 8 rows for experts with more than 8).
 #include <stdint.h>
 
 #include "internal.h"
@@ -24,8 +24,12 @@ namespace {
 
 using namespace mma;
 
-constexpr int kWN = 8;           // warps (32-column slices) per CTA
-constexpr int kRowsPerPass = 16; // rows of one expert per pass over a weight tile
+constexpr int kWN = 8;           // warps (64-column slices) per CTA
+constexpr int kCH = 2;           // 16-byte chunks per lane per group
+constexpr int kRowsPerPass = 8;  // rows of one expert per pass over a weight tile
+
+template <int NB>
+using MoeGeo = Geo<NB, kCH, kWN, 4, 24576>;
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -123,54 +127,53 @@ struct GroupedArgs {
   const int* hdr;
   const int* off;
   const int* active;
-  const int32_t* qw;         // [E, Kr/8, N]
-  const float* sc;           // [E, Kr/32, N]
   int N;                     // columns per expert (gate/up: 2I)
   int Kr;                    // reduction length (gate/up: K; down: I)
   int tiles;
   float* dst;                // gate/up: h [P, I]; down: y_pair [P, K]
   int ldd;
+  unsigned int* err;
 };
 
 template <int NB, bool SWIGLU>
-__device__ __forceinline__ void grouped_pass(const GroupedArgs& a, const int32_t* qw,
-                                             const float* sc, int tile, int row0, int rows,
-                                             char* smem) {
+__device__ __forceinline__ void grouped_pass(const GroupedArgs& a, const CUtensorMap* tq,
+                                             const CUtensorMap* ts, int e, int tile, int row0,
+                                             int rows, char* smem, int& seq) {
   const int warp = threadIdx.x >> 5;
   auto rowptr = [&](int m) {
     const int p = row0 + m;
     const int r = a.gather ? (a.sorted_pair[p] / a.topk) : p;
     return a.src + (size_t)r * a.Kr;
   };
-  float acc[2][NB][4];
-  stream_groups<NB, SWIGLU, kWN>(rowptr, rows, qw, sc, a.N, 0, a.Kr / kGroup, tile * kWN, smem,
-                                 acc);
-  store_direct<NB, SWIGLU>(acc, tile * kWN + warp, a.N, rows, a.dst + (size_t)row0 * a.ldd);
+  float acc[kCH][2][NB][4];
+  stream_groups<NB, kCH, SWIGLU, kWN, MoeGeo<NB>>(rowptr, rows, tq, ts, e, a.N, 0,
+                                                   a.Kr / kGroup, tile * kWN, smem, seq, a.err,
+                                                   acc);
+  store_direct<NB, kCH, SWIGLU>(acc, tile * kWN + warp, a.N, rows, a.dst + (size_t)row0 * a.ldd);
 }
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(kWN * 32, 2) moe_grouped_kernel(GroupedArgs a) {
-  extern __shared__ __align__(128) char smem[];
+__global__ void __launch_bounds__(kWN * 32, 2)
+    moe_grouped_kernel(const __grid_constant__ CUtensorMap tq,
+                       const __grid_constant__ CUtensorMap ts, GroupedArgs a) {
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = align1024(smem_raw);
+  init_barriers<MoeGeo<2>>(smem, kWN);
+  int seq = 0;
   const int n_active = a.hdr[0];
   const long long total = (long long)n_active * a.tiles;
-  const size_t qstride = (size_t)(a.Kr / 8) * a.N;
-  const size_t sstride = (size_t)(a.Kr / kGroup) * a.N;
   for (long long item = blockIdx.x; item < total; item += gridDim.x) {
     const int ai = (int)(item / a.tiles);
     const int tile = (int)(item - (long long)ai * a.tiles);
     const int e = a.active[ai];
     const int r0 = a.off[e];
     const int rows = a.off[e + 1] - r0;
-    const int32_t* qw = a.qw + (size_t)e * qstride;
-    const float* sc = a.sc + (size_t)e * sstride;
     for (int c0 = 0; c0 < rows; c0 += kRowsPerPass) {
       const int mr = (rows - c0) < kRowsPerPass ? (rows - c0) : kRowsPerPass;
-      switch ((mr + 3) >> 2) {
-        case 1: grouped_pass<1, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
-        case 2: grouped_pass<2, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
-        case 3: grouped_pass<3, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
-        default: grouped_pass<4, SWIGLU>(a, qw, sc, tile, r0 + c0, mr, smem); break;
-      }
+      if (mr <= 4)
+        grouped_pass<1, SWIGLU>(a, &tq, &ts, e, tile, r0 + c0, mr, smem, seq);
+      else
+        grouped_pass<2, SWIGLU>(a, &tq, &ts, e, tile, r0 + c0, mr, smem, seq);
     }
   }
 }
@@ -217,21 +220,35 @@ __global__ void topk_softmax_kernel(const float* __restrict__ logits, float* __r
   }
 }
 
+// Both NB paths of the grouped kernel share one shared-memory buffer (the larger layout); the
+// rings and barriers sit at the same offsets in both.
+static_assert(MoeGeo<1>::kBarOff == MoeGeo<2>::kBarOff, "shared barrier offset");
+constexpr int kMoeSmem =
+    MoeGeo<2>::kAlloc > MoeGeo<1>::kAlloc ? MoeGeo<2>::kAlloc : MoeGeo<1>::kAlloc;
+
 template <bool SWIGLU>
-cudaError_t launch_grouped(const GroupedArgs& a, const DeviceInfo& di, cudaStream_t s) {
+cudaError_t launch_grouped(const GroupedArgs& a, const int32_t* qw, const float* sc, int E,
+                           const DeviceInfo& di, cudaStream_t s) {
   static int occ_cache[64] = {0};
   auto kern = moe_grouped_kernel<SWIGLU>;
-  constexpr int smem = Smem<4, kWN>::kBytes;
   int& occ = occ_cache[di.device & 63];
   if (occ == 0) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoeSmem);
     if (e != cudaSuccess) return e;
     int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kWN * 32, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kWN * 32, kMoeSmem);
     if (e != cudaSuccess) return e;
     occ = o < 1 ? 1 : o;
   }
-  kern<<<di.sm_count * occ, kWN * 32, smem, s>>>(a);
+  CUtensorMap tq, ts;
+  cudaError_t e = make_tmap(&tq, 0, qw, (uint64_t)a.N, (uint64_t)(a.Kr / 8), (uint64_t)E, 32,
+                            kRows);
+  if (e != cudaSuccess) return e;
+  e = make_tmap(&ts, 1, sc, (uint64_t)a.N, (uint64_t)(a.Kr / kGroup), (uint64_t)E, 32,
+                kRows / 4);
+  if (e != cudaSuccess) return e;
+  kern<<<di.sm_count * occ, kWN * 32, kMoeSmem, s>>>(tq, ts, a);
   return cudaGetLastError();
 }
 
@@ -273,26 +290,23 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
   gu.hdr = hdr;
   gu.off = off;
   gu.active = active;
-  gu.qw = qw_gu;
-  gu.sc = sc_gu;
+  gu.err = device_error_word();
   gu.N = 2 * I;
   gu.Kr = K;
-  gu.tiles = ((I + 15) / 16 + kWN - 1) / kWN;
+  gu.tiles = ((I + 16 * kCH - 1) / (16 * kCH) + kWN - 1) / kWN;
   gu.dst = h;
   gu.ldd = I;
-  if ((e = launch_grouped<true>(gu, di, s)) != cudaSuccess) return e;
+  if ((e = launch_grouped<true>(gu, qw_gu, sc_gu, E, di, s)) != cudaSuccess) return e;
 
   GroupedArgs dn = gu;
   dn.src = h;
   dn.gather = false;
-  dn.qw = qw_dn;
-  dn.sc = sc_dn;
   dn.N = K;
   dn.Kr = I;
-  dn.tiles = ((K + 31) / 32 + kWN - 1) / kWN;
+  dn.tiles = ((K + 32 * kCH - 1) / (32 * kCH) + kWN - 1) / kWN;
   dn.dst = ypair;
   dn.ldd = K;
-  if ((e = launch_grouped<false>(dn, di, s)) != cudaSuccess) return e;
+  if ((e = launch_grouped<false>(dn, qw_dn, sc_dn, E, di, s)) != cudaSuccess) return e;
 
   const long long total4 = (long long)T * (K / 4);
   long long blocks = (total4 + 255) / 256;

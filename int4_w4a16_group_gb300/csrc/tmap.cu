@@ -1,0 +1,93 @@
+// Host-side TMA descriptors (CUtensorMap) for the packed weights and scales.
+//
+// The driver function that encodes a descriptor is looked up once through the runtime, so the
+// library does not link against libcuda (it still loads on machines without a GPU driver).
+// Descriptors embed the global address, so they are built per call; a small per-thread cache
+// returns the previous descriptor when the same tensor is used again.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "internal.h"
+
+namespace w4a16 {
+namespace {
+
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                              const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                              const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                              CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeFn g_encode = nullptr;
+std::once_flag g_encode_once;
+cudaError_t g_encode_status = cudaSuccess;
+
+void load_encode() {
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                   cudaEnableDefault, &q);
+  if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) {
+    g_encode_status = (e != cudaSuccess) ? e : cudaErrorNotSupported;
+    return;
+  }
+  g_encode = reinterpret_cast<EncodeFn>(fn);
+}
+
+struct CacheEntry {
+  const void* ptr;
+  uint64_t d0, d1, d2;
+  uint32_t b0, b1;
+  int kind;
+  CUtensorMap map;
+};
+constexpr int kCacheSize = 8;
+thread_local CacheEntry t_cache[kCacheSize];
+thread_local int t_next = 0;
+
+}  // namespace
+
+// 3-D tiled descriptor of a row-major [d2][d1][d0] tensor of 4-byte elements (d0 contiguous),
+// box (b0 x b1 x 1). kind 0: packed codes (int32, 128-byte swizzle); kind 1: scales (float32,
+// no swizzle). Out-of-range box elements read as zero.
+cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint32_t b0, uint32_t b1) {
+  for (int i = 0; i < kCacheSize; ++i) {
+    const CacheEntry& c = t_cache[i];
+    if (c.ptr == base && c.d0 == d0 && c.d1 == d1 && c.d2 == d2 && c.b0 == b0 && c.b1 == b1 &&
+        c.kind == kind) {
+      *out = c.map;
+      return cudaSuccess;
+    }
+  }
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return g_encode_status;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  const cuuint32_t box[3] = {b0, b1, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  CUtensorMap m;
+  memset(&m, 0, sizeof(m));
+  const CUresult r = g_encode(
+      &m, kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+      const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+  CacheEntry& c = t_cache[t_next];
+  t_next = (t_next + 1) % kCacheSize;
+  c.ptr = base;
+  c.d0 = d0;
+  c.d1 = d1;
+  c.d2 = d2;
+  c.b0 = b0;
+  c.b1 = b1;
+  c.kind = kind;
+  c.map = m;
+  *out = m;
+  return cudaSuccess;
+}
+
+}  // namespace w4a16
