@@ -52,16 +52,20 @@ def _stale(target: str, deps: list[str]) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile (when stale) and link libw4a16.so; returns its path."""
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          out: str | None = None, build_dir: str | None = None) -> str:
+    """Compile (when stale) and link libw4a16.so (or `out`, with objects in `build_dir`);
+    returns the library path."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    lib = out or LIB
+    bdir = build_dir or BUILD
+    os.makedirs(bdir, exist_ok=True)
     hdrs = _headers()
     flags = NVCC_FLAGS + (extra_flags or [])
     jobs = []
     objs = []
     for src in sources():
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
         objs.append(obj)
         if force or _stale(obj, [src] + hdrs + [__file__]):
             jobs.append([nvcc, *flags, "-c", src, "-o", obj])
@@ -78,11 +82,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     if jobs:
         with cf.ThreadPoolExecutor(max_workers=min(len(jobs), os.cpu_count() or 4)) as ex:
             list(ex.map(run, jobs))
-    if force or jobs or _stale(LIB, objs):
-        tmp = LIB + ".tmp"
+    if force or jobs or _stale(lib, objs):
+        tmp = lib + ".tmp"
         run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"])
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 def main(argv=None):

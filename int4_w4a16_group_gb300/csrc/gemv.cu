@@ -21,65 +21,43 @@ namespace {
 
 using namespace mma;
 
-// Warps (slices) per CTA: small CTAs for up to 8 rows (several per SM, clusters pack easily),
-// 8 warps for 9..16 rows.
-template <int NB>
-struct Warps {
-  static constexpr int value = NB <= 2 ? 4 : 8;
-};
+// Geometry of the two orientations.
+//   up to 8 rows : A = codes; 4-warp CTAs, 2-stage rings and a 12-16 KB activation budget keep
+//                  a CTA near 53 KB so four fit per SM (16 warps, ~80 KB of copies in flight);
+//   9..16 rows   : A = activations (no padded MMA rows); 4-warp CTAs, 3-stage rings, 16 KB.
+constexpr int kWN = 4;  // warps (slices) per CTA
 
-// Ring depth and activation budget: 2 stages and 12 KB keep a 4-warp CTA near 53 KB, so four
-// fit per SM (16 warps, ~80 KB of copies in flight); 8-warp CTAs keep 4 stages.
+// Tuning knobs (compile-time; defaults are the measured best on GB300).
+#ifndef W4A16_CODES_RING
+#define W4A16_CODES_RING 2
+#endif
+#ifndef W4A16_CODES_MINB
+#define W4A16_CODES_MINB 4
+#endif
+#ifndef W4A16_ACTS_RING
+#define W4A16_ACTS_RING 3
+#endif
+#ifndef W4A16_ACTS_MINB
+#define W4A16_ACTS_MINB 4
+#endif
+#ifndef W4A16_WIDE_CH
+#define W4A16_WIDE_CH 4
+#endif
+
 template <int NB, int CH>
-using DenseGeo = Geo<NB, CH, Warps<NB>::value, NB <= 2 ? 2 : 4, NB <= 2 ? 12288 : 24576>;
+using CodesGeo = Geo<NB, CH, kWN, W4A16_CODES_RING, NB == 1 ? 12288 : 16384>;
+template <int CH>
+using ActsGeo = Geo<4, CH, kWN, W4A16_ACTS_RING, 16384>;
 
-template <int NB, int CH, bool SWIGLU>
-__global__ void __launch_bounds__(Warps<NB>::value * 32, NB <= 2 ? 4 : 2)
-    gemv_mma_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
-                    const float* __restrict__ x, float* __restrict__ y, int M, int N, int K,
-                    unsigned int* err) {
-  constexpr int kWN = Warps<NB>::value;
-  extern __shared__ __align__(1024) char smem_raw[];
-  char* smem = align1024(smem_raw);
-  cg::cluster_group cluster = cg::this_cluster();
-  const int tile = blockIdx.x;
+// Split-K epilogue shared by both orientations: every CTA of the cluster has written its
+// partial tile red[4*NBR rows][kCols] (SwiGLU: kOut gate sums, then kOut up sums); rank r
+// finishes its share of the columns over all ranks in rank order.
+template <bool SWIGLU, int kCols>
+__device__ __forceinline__ void cluster_finish(cg::cluster_group& cluster, float* red, int tile,
+                                               int M, int N, float* y) {
+  constexpr int kOut = kCols / 2;
   const int CK = (int)cluster.dim_blocks().y;
   const int rank = (int)cluster.block_index().y;
-  const int warp = threadIdx.x >> 5;
-  const int G = K / kGroup;
-  const int q0 = (int)((long long)rank * G / CK);
-  const int q1 = (int)((long long)(rank + 1) * G / CK);
-
-  using L = DenseGeo<NB, CH>;
-  init_barriers<L>(smem, kWN);
-  float acc[CH][2][NB][4];
-  int seq = 0;
-  auto rowptr = [&](int m) { return x + (size_t)m * K; };
-  stream_groups<NB, CH, SWIGLU, kWN, L>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN,
-                                        smem, seq, err, acc);
-
-  if (CK == 1) {
-    store_direct<NB, CH, SWIGLU>(acc, tile * kWN + warp, N, M, y);
-    return;
-  }
-  // Split-K: partial tile [4*NB rows][kCols local columns] in shared memory (reusing the
-  // code ring), then rank r finishes its share of the columns over all ranks in order.
-  // SwiGLU tiles hold the kOut gate sums first, then the kOut matching up sums.
-  constexpr int kCols = kWN * 32 * CH;
-  constexpr int kOut = kWN * 16 * CH;
-  static_assert(4 * NB * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
-                "split-K tile must fit in the code ring");
-  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
-  {
-    const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-    for (int c = 0; c < CH; ++c)
-#pragma unroll
-      for (int b = 0; b < NB; ++b)
-        *reinterpret_cast<float4*>(&red[(4 * b + t) * kCols +
-                                        tile_local_col<CH, SWIGLU, kWN>(warp, c, g)]) =
-            chunk_result<NB, CH>(acc, c, b);
-  }
   cluster.sync();
   if (SWIGLU) {
     const int I = N >> 1;
@@ -110,6 +88,101 @@ __global__ void __launch_bounds__(Warps<NB>::value * 32, NB <= 2 ? 4 : 2)
   cluster.sync();  // peers may still be reading this CTA's shared memory
 }
 
+template <int NB, int CH, bool SWIGLU>
+__global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
+    gemv_codes_kernel(const __grid_constant__ CUtensorMap tq,
+                      const __grid_constant__ CUtensorMap ts, const float* __restrict__ x,
+                      float* __restrict__ y, int M, int N, int K, unsigned int* err) {
+  using L = CodesGeo<NB, CH>;
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = align1024(smem_raw);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tile = blockIdx.x;
+  const int CK = (int)cluster.dim_blocks().y;
+  const int rank = (int)cluster.block_index().y;
+  const int warp = threadIdx.x >> 5;
+  const int G = K / kGroup;
+  const int q0 = (int)((long long)rank * G / CK);
+  const int q1 = (int)((long long)(rank + 1) * G / CK);
+
+  init_barriers<L>(smem, kWN);
+  float acc[CH][2][NB][4];
+  int seq = 0;
+  auto rowptr = [&](int m) { return x + (size_t)m * K; };
+  stream_groups<NB, CH, SWIGLU, kWN, L>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN,
+                                        smem, seq, err, acc);
+  if (CK == 1) {
+    store_direct<NB, CH, SWIGLU>(acc, tile * kWN + warp, N, M, y);
+    return;
+  }
+  constexpr int kCols = kWN * 32 * CH;
+  static_assert(4 * NB * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
+                "split-K tile must fit in the code ring");
+  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+      *reinterpret_cast<float4*>(&red[(4 * b + t) * kCols +
+                                      tile_local_col<CH, SWIGLU, kWN>(warp, c, g)]) =
+          chunk_result<NB, CH>(acc, c, b);
+  cluster_finish<SWIGLU, kCols>(cluster, red, tile, M, N, y);
+}
+
+template <int CH, bool SWIGLU>
+__global__ void __launch_bounds__(kWN * 32, W4A16_ACTS_MINB)
+    gemv_acts_kernel(const __grid_constant__ CUtensorMap tq,
+                     const __grid_constant__ CUtensorMap ts, const float* __restrict__ x,
+                     float* __restrict__ y, int M, int N, int K, unsigned int* err) {
+  using L = ActsGeo<CH>;
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = align1024(smem_raw);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tile = blockIdx.x;
+  const int CK = (int)cluster.dim_blocks().y;
+  const int rank = (int)cluster.block_index().y;
+  const int warp = threadIdx.x >> 5;
+  const int G = K / kGroup;
+  const int q0 = (int)((long long)rank * G / CK);
+  const int q1 = (int)((long long)(rank + 1) * G / CK);
+
+  init_barriers<L>(smem, kWN);
+  float acc[CH][4][4];
+  int seq = 0;
+  auto rowptr = [&](int m) { return x + (size_t)m * K; };
+  stream_groups_xa<CH, SWIGLU, kWN, L>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN, smem,
+                                       seq, err, acc);
+  if (CK == 1) {
+    store_direct_xa<CH, SWIGLU>(acc, tile * kWN + warp, N, M, y);
+    return;
+  }
+  constexpr int kCols = kWN * 32 * CH;
+  static_assert(16 * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
+                "split-K tile must fit in the code ring");
+  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int hh[2] = {lane_chunk(2 * t), lane_chunk(2 * t + 1)};
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        // tile_local_col with the lane chunk of B column 2t + e
+        int lc;
+        if (SWIGLU) {
+          constexpr int H = CH / 2;
+          lc = (c >= H ? kWN * 16 * CH : 0) + warp * 16 * CH + 32 * (c >= H ? c - H : c) +
+               4 * hh[e];
+        } else {
+          lc = warp * 32 * CH + 32 * c + 4 * hh[e];
+        }
+        *reinterpret_cast<float4*>(&red[(g + 8 * hf) * kCols + lc]) = xa_result<CH>(acc, c, hf, e);
+      }
+  cluster_finish<SWIGLU, kCols>(cluster, red, tile, M, N, y);
+}
+
 constexpr int kMaxCluster = 16;
 
 struct LaunchCache {
@@ -118,20 +191,18 @@ struct LaunchCache {
   int max_clusters[kMaxCluster + 1] = {0};  // index = cluster size
 };
 
-// Slices (one warp each) of a problem for CH chunks per lane.
+// Slices (one warp each) of a problem for CH tiles per warp.
 template <int CH, bool SWIGLU>
 int slices_of(int N) {
   return SWIGLU ? ((N >> 1) + 16 * CH - 1) / (16 * CH) : (N + 32 * CH - 1) / (32 * CH);
 }
 
-template <int NB, int CH, bool SWIGLU>
-cudaError_t launch_cfg(const float* x, const int32_t* qw, const float* sc, float* y, int M,
-                       int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  constexpr int kWN = Warps<NB>::value;
-  static LaunchCache cache;
-  auto kern = gemv_mma_kernel<NB, CH, SWIGLU>;
-  constexpr int smem = DenseGeo<NB, CH>::kAlloc;
-  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
+// Launches `kern` over tiles x CK clusters, CK chosen so that the waves of clusters fill the GPU
+// most evenly (each CTA keeps at least 8 groups of K).
+template <typename Kern>
+cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, const float* x,
+                         const int32_t* qw, const float* sc, float* y, int M, int N, int K,
+                         const DeviceInfo& di, cudaStream_t s) {
   const int G = K / kGroup;
   const int bit = 1 << (di.device & 31);
   if (!(cache.device_mask & bit)) {
@@ -164,8 +235,6 @@ cudaError_t launch_cfg(const float* x, const int32_t* qw, const float* sc, float
     }
     cache.device_mask |= bit;
   }
-  // Pick the K split whose waves of clusters fill the GPU most evenly; each CTA keeps at
-  // least 8 groups of K.
   const double slots = (double)di.sm_count * cache.occ;
   int CK = 1;
   double best = -1.0;
@@ -200,23 +269,36 @@ cudaError_t launch_cfg(const float* x, const int32_t* qw, const float* sc, float
   return cudaLaunchKernelEx(&cfg, kern, tq, ts, x, y, M, N, K, device_error_word());
 }
 
+template <int NB, int CH, bool SWIGLU>
+cudaError_t launch_codes(const float* x, const int32_t* qw, const float* sc, float* y, int M,
+                         int N, int K, const DeviceInfo& di, cudaStream_t s) {
+  static LaunchCache cache;
+  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
+  return launch_split(gemv_codes_kernel<NB, CH, SWIGLU>, CodesGeo<NB, CH>::kAlloc, cache, tiles,
+                      x, qw, sc, y, M, N, K, di, s);
+}
+
+template <int CH, bool SWIGLU>
+cudaError_t launch_acts(const float* x, const int32_t* qw, const float* sc, float* y, int M,
+                        int N, int K, const DeviceInfo& di, cudaStream_t s) {
+  static LaunchCache cache;
+  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
+  return launch_split(gemv_acts_kernel<CH, SWIGLU>, ActsGeo<CH>::kAlloc, cache, tiles, x, qw, sc,
+                      y, M, N, K, di, s);
+}
+
 // Up to 4 rows: 4 tiles per warp (128 columns) when the problem is wide enough to give every
-// SM several warps, else 2; 5..8 rows: 2; 9..16 rows: 1 (2 with the fused SwiGLU, which pairs
-// gate and up tiles), for the register budget.
+// SM several warps, else 2; 5..8 rows: 2; 9..16 rows: the activations-as-A kernel, 2 tiles.
 template <bool SWIGLU>
 cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
                      int K, const DeviceInfo& di, cudaStream_t s) {
   const bool wide = slices_of<4, SWIGLU>(N) * 8 >= 2 * di.sm_count;
-  constexpr int CH_BIG = SWIGLU ? 2 : 1;
-  switch ((M + 3) / 4) {
-    case 1:
-      return wide ? launch_cfg<1, 4, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
-                  : launch_cfg<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    case 2: return launch_cfg<2, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    case 3: return launch_cfg<3, CH_BIG, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    case 4: return launch_cfg<4, CH_BIG, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-    default: return cudaErrorInvalidValue;
-  }
+  if (M <= 4)
+    return wide ? launch_codes<1, W4A16_WIDE_CH, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
+                : launch_codes<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+  if (M <= 8) return launch_codes<2, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+  if (M <= 16) return launch_acts<2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace

@@ -71,13 +71,15 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
                : "memory");
 }
-__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+// One bounded wait step: the thread sleeps until phase `parity` of the barrier completes or
+// about `hint_ns` pass (no busy spinning), and reports whether the phase completed.
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
       : "memory");
   return ok != 0;
 }
@@ -86,11 +88,14 @@ __device__ __forceinline__ uint64_t global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
   return t;
 }
-// Waits for phase `parity` of the barrier; gives up after `limit_ns` and returns false.
+// Waits for phase `parity` of the barrier, sleeping in steps of at most 1 ms; gives up once
+// `limit_ns` of wall time have passed and returns false. The clock is read only after a
+// step that ended without the phase completing.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
-  if (mbar_try_wait(bar, parity)) return true;
+  constexpr uint32_t kStepNs = 1000000u;
+  if (mbar_try_wait(bar, parity, kStepNs)) return true;
   const uint64_t t0 = global_ns();
-  while (!mbar_try_wait(bar, parity)) {
+  while (!mbar_try_wait(bar, parity, kStepNs)) {
     if (global_ns() - t0 > limit_ns) return false;
   }
   return true;
@@ -114,13 +119,14 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 
-// Tensor-core product with a zero accumulator input (no register moves to clear d).
+// Tensor-core product with the accumulator input taken from a loop-invariant zero quad.
 __device__ __forceinline__ void mma_f16_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
-                                           uint32_t b1, float zero) {
+                                           uint32_t b1, const float (&z)[4]) {
   asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-      "{%8,%9}, {%10,%10,%10,%10};\n"
+      "{%8,%9}, {%10,%11,%12,%13};\n"
       : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
-      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(zero));
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z[0]), "f"(z[1]),
+        "f"(z[2]), "f"(z[3]));
 }
 
 // (a & mask) | 0x64006400 in one LOP3.
@@ -150,6 +156,24 @@ __device__ __forceinline__ void unpack_word(uint32_t w, uint32_t (&p)[4]) {
   p[3] = hfma2_u32(lop_and_or(w8, 0x00F000F0u), SIXTEENTH, M72);
 }
 
+// Two words (columns of A rows g and g + 8) -> the A fragments of both k-steps, written in
+// operand order so no register moves are needed:
+//   a0 = (n0 n4 of wa, n0 n4 of wb, n1 n5 of wa, n1 n5 of wb), a1 = the same for n2 n6 / n3 n7.
+__device__ __forceinline__ void unpack_pair(uint32_t wa, uint32_t wb, uint32_t (&a0)[4],
+                                            uint32_t (&a1)[4]) {
+  const uint32_t ONE = 0x3C003C00u, SIXTEENTH = 0x2C002C00u;
+  const uint32_t M1032 = 0xE408E408u, M72 = 0xD480D480u;
+  const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+  a0[0] = hfma2_u32(lop_and_or(wa, 0x000F000Fu), ONE, M1032);
+  a0[1] = hfma2_u32(lop_and_or(wb, 0x000F000Fu), ONE, M1032);
+  a0[2] = hfma2_u32(lop_and_or(wa, 0x00F000F0u), SIXTEENTH, M72);
+  a0[3] = hfma2_u32(lop_and_or(wb, 0x00F000F0u), SIXTEENTH, M72);
+  a1[0] = hfma2_u32(lop_and_or(wa8, 0x000F000Fu), ONE, M1032);
+  a1[1] = hfma2_u32(lop_and_or(wb8, 0x000F000Fu), ONE, M1032);
+  a1[2] = hfma2_u32(lop_and_or(wa8, 0x00F000F0u), SIXTEENTH, M72);
+  a1[3] = hfma2_u32(lop_and_or(wb8, 0x00F000F0u), SIXTEENTH, M72);
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -160,15 +184,15 @@ __device__ __forceinline__ float exp2i(int e) { return __int_as_float((e + 127) 
 
 // ------------------------------------------------------------------------------ activations
 
-// One warp prepares the B fragments of one group q (inputs 32q .. 32q + 31) for rows
-// 0 .. M-1 (rows >= M are zero): writes NB x 512 B at dst and the group's 2^e at *fscale.
+// Preparing the B fragments of one group q (inputs 32q .. 32q + 31) for rows 0 .. M-1 (rows
+// >= M are zero) takes two steps so the loads can be issued long before their use:
+//   prep_load : lane (g, t) loads x[m][32q + 8t .. +7] for m = 4b + g/2 into registers;
+//   prep_store: the warp finds the group's largest magnitude, scales by 2^-e, splits into fp16
+//               hi/lo terms and writes NB x 512 B at dst plus the group's 2^e at *fscale.
 // rowptr(m) returns a pointer to row m of x (float32, 16-byte aligned).
 template <int NB, typename RowPtr>
-__device__ __forceinline__ void prep_group(const RowPtr& rowptr, int M, int q, char* dst,
-                                           float* fscale) {
+__device__ __forceinline__ void prep_load(const RowPtr& rowptr, int M, int q, float (&v)[NB][8]) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  float v[NB][8];
-  float amax = 0.0f;
 #pragma unroll
   for (int b = 0; b < NB; ++b) {
     const int m = 4 * b + (g >> 1);
@@ -181,16 +205,29 @@ __device__ __forceinline__ void prep_group(const RowPtr& rowptr, int M, int q, c
 #pragma unroll
       for (int j = 0; j < 8; ++j) v[b][j] = 0.0f;
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[b][j]));
   }
+}
+
+// Power-of-two exponent e of a group: its largest magnitude times 2^-e lies in [2^14, 2^15),
+// far from fp16 overflow (65504) and with the lo term of every element within 2^17 of it
+// still a normal fp16 number. (Warp-wide: every lane passes its own partial maximum.)
+__device__ __forceinline__ int group_exponent(float amax) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-  // Scale so that the group's largest magnitude lands in [2^14, 2^15): far from fp16
-  // overflow (65504) and with the lo term of every element within 2^17 of it still normal.
   int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
   if (amax == 0.0f) ex = 0;
-  ex = ex < -110 ? -110 : (ex > 110 ? 110 : ex);
+  return ex < -110 ? -110 : (ex > 110 ? 110 : ex);
+}
+
+template <int NB>
+__device__ __forceinline__ void prep_store(const float (&v)[NB][8], char* dst, float* fscale) {
+  const int lane = threadIdx.x & 31, g = lane >> 2;
+  float amax = 0.0f;
+#pragma unroll
+  for (int b = 0; b < NB; ++b)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[b][j]));
+  const int ex = group_exponent(amax);
   const float up = exp2i(14 - ex);
   const bool lo_term = (g & 1) != 0;
 #pragma unroll
@@ -215,6 +252,11 @@ __device__ __forceinline__ void prep_group(const RowPtr& rowptr, int M, int q, c
 // ------------------------------------------------------------------------------ geometry
 
 constexpr int kRows = 8;     // packed rows per stage (2 groups)
+
+#ifndef W4A16_UNROLL_GROUPS
+#define W4A16_UNROLL_GROUPS 2
+#endif
+constexpr int kUnrollGroups = W4A16_UNROLL_GROUPS;  // groups of a stage interleaved by the compiler
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // give up a barrier wait after 2 s
 
 // Shared-memory layout of one CTA (offsets from a 1024-byte aligned base). Everything up to
@@ -347,22 +389,23 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
     for (int s = 0; s < kRing - 1 && s < nst; ++s) issue(s);
   }
 
-  // Activation fragments: everything at once when it fits, else alternating halves.
-  const int pg = nq <= L::kXGroups ? ((nq + 1) & ~1) : L::kXGroups / 2;
-  auto prep_chunk = [&](int pc, int buf) {
-    for (int j = warp; j < pg; j += WN) {
-      const int qi = pc * pg + j;
-      if (qi < nq)
-        prep_group<NB>(rowptr, M, q0 + qi, xbuf + (buf * pg + j) * NB * kXChunkBytes,
-                       &fsc[buf * pg + j]);
+  // Activation fragments: the whole range at once when it fits; otherwise chunks of WN groups
+  // (one per warp), double-buffered, whose loads are issued before the previous chunk's
+  // compute and converted after it.
+  static_assert(L::kXGroups >= 2 * WN && WN % 2 == 0, "x region must hold two chunks");
+  const int pg = nq <= L::kXGroups ? ((nq + 1) & ~1) : WN;
+  for (int j = warp; j < pg; j += WN) {
+    if (j < nq) {
+      float v[NB][8];
+      prep_load<NB>(rowptr, M, q0 + j, v);
+      prep_store<NB>(v, xbuf + j * NB * kXChunkBytes, &fsc[j]);
     }
-  };
-  prep_chunk(0, 0);
+  }
   __syncthreads();
 
   bool ok = true;
   int fail_s = 0;
-  const float zero = 0.0f;
+  const float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
   const uint32_t xbuf_s = smem_u32(xbuf) + lane * 16;
   const uint32_t fsc_s = smem_u32(fsc);
   const int h = lane_chunk(g);
@@ -370,7 +413,11 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
   const int sps = pg >> 1;  // stages per x chunk
   for (int pc = 0; pc < nchunks; ++pc) {
     const int buf = pc & 1;
-    if (pc + 1 < nchunks) prep_chunk(pc + 1, buf ^ 1);
+    // Next chunk's activations: loads now, conversion after this chunk's compute.
+    float nv[NB][8];
+    const int qn = (pc + 1) * pg + warp;
+    const bool more = pc + 1 < nchunks && qn < nq;
+    if (more) prep_load<NB>(rowptr, M, q0 + qn, nv);
     const int s_end = ((pc + 1) * sps < nst) ? (pc + 1) * sps : nst;
     if (any) {
       for (int s = pc * sps; s < s_end; ++s) {
@@ -386,7 +433,7 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
           }
         }
         if (ok) {
-#pragma unroll
+#pragma unroll (kUnrollGroups)
           for (int j = 0; j < 2; ++j) {
             const int qi = 2 * s + j;
             if (qi < nq) {
@@ -409,22 +456,15 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
               for (int b = 0; b < NB; ++b) bf[b] = lds128(xbuf_s + (xi * NB + b) * kXChunkBytes);
 #pragma unroll
               for (int c = 0; c < CH; ++c) {
-                uint32_t p[4][4];
-                unpack_word(wq[c].x, p[0]);
-                unpack_word(wq[c].y, p[1]);
-                unpack_word(wq[c].z, p[2]);
-                unpack_word(wq[c].w, p[3]);
                 const float sv[4] = {s4[c].x * fg, s4[c].y * fg, s4[c].z * fg, s4[c].w * fg};
 #pragma unroll
                 for (int T = 0; T < 2; ++T) {
-                  const uint32_t a0[4] = {p[2 * T][0], p[2 * T + 1][0], p[2 * T][1],
-                                          p[2 * T + 1][1]};
-                  const uint32_t a1[4] = {p[2 * T][2], p[2 * T + 1][2], p[2 * T][3],
-                                          p[2 * T + 1][3]};
+                  uint32_t a0[4], a1[4];
+                  unpack_pair(T ? wq[c].z : wq[c].x, T ? wq[c].w : wq[c].y, a0, a1);
 #pragma unroll
                   for (int b = 0; b < NB; ++b) {
                     float d[4];
-                    mma_f16_zc(d, a0, bf[b].x, bf[b].y, zero);
+                    mma_f16_zc(d, a0, bf[b].x, bf[b].y, zq);
                     mma_f16(d, a1, bf[b].z, bf[b].w);
                     acc[c][T][b][0] = fmaf(sv[2 * T], d[0], acc[c][T][b][0]);
                     acc[c][T][b][1] = fmaf(sv[2 * T], d[1], acc[c][T][b][1]);
@@ -439,6 +479,9 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
         __syncwarp();  // every lane is done with stage st before lane 0 refills it
       }
     }
+    if (more)
+      prep_store<NB>(nv, xbuf + ((buf ^ 1) * pg + warp) * NB * kXChunkBytes,
+                     &fsc[(buf ^ 1) * pg + warp]);
     if (nchunks > 1) __syncthreads();
   }
   if (any && !ok) {
@@ -515,6 +558,264 @@ __device__ __forceinline__ int tile_local_col(int warp, int c, int g) {
     return (c >= H ? WN * SO : 0) + warp * SO + 32 * (c >= H ? c - H : c) + h4;
   }
   return warp * 32 * CH + 32 * c + h4;
+}
+
+// ------------------------------------------------------------------------------ 9..16 rows
+//
+// For 9..16 activation rows the roles swap: A (16 x 16) = activations (rows m = g and g + 8),
+// B (16 x 8) = codes, so the hi and lo activation terms are two A operands accumulating into
+// the same C and no MMA row is padding. B column n of n8-tile i is weight column 4 h(n) + i of
+// the 32-column tile: lane (g, t) loads chunk h(g) (columns 4h .. 4h + 3) of packed row 4q + t,
+// and word i of it is its B fragment for n8-tile i (k-slots as in the other orientation).
+// C: lane (g, t) holds rows g, g + 8 and B columns 2t, 2t + 1 of each n8-tile i, i.e. weight
+// columns 4 h(2t) + i and 4 h(2t + 1) + i.
+
+// Preparing the A fragments of group q for rows 0 .. M-1 (M <= 16; others zero), in two steps
+// as for the other orientation. Output: 4 x 512 B at dst, chunk (term * 2 + kstep), each an
+// A operand quad in register order: (row g pair 2ks, row g+8 pair 2ks, row g pair 2ks+1,
+// row g+8 pair 2ks+1), pair p of a row = inputs (8t + p, 8t + p + 4); term 0 = hi, 1 = lo.
+template <typename RowPtr>
+__device__ __forceinline__ void prep_load_xa(const RowPtr& rowptr, int M, int q, float (&v)[2][8]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int m = g + 8 * hf;
+    if (m < M) {
+      const float4* p = reinterpret_cast<const float4*>(rowptr(m) + 32 * q + 8 * t);
+      const float4 u0 = __ldg(p), u1 = __ldg(p + 1);
+      v[hf][0] = u0.x; v[hf][1] = u0.y; v[hf][2] = u0.z; v[hf][3] = u0.w;
+      v[hf][4] = u1.x; v[hf][5] = u1.y; v[hf][6] = u1.z; v[hf][7] = u1.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[hf][j] = 0.0f;
+    }
+  }
+}
+
+__device__ __forceinline__ void prep_store_xa(const float (&v)[2][8], char* dst, float* fscale) {
+  const int lane = threadIdx.x & 31;
+  float amax = 0.0f;
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) amax = fmaxf(amax, fabsf(v[hf][j]));
+  const int ex = group_exponent(amax);
+  const float up = exp2i(14 - ex);
+  uint32_t ph[2][4], pl[2][4];  // [half][pair]
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    float hi[8], lo[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const float xs = v[hf][j] * up;
+      hi[j] = __half2float(__float2half_rn(xs));
+      lo[j] = xs - hi[j];
+    }
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+      ph[hf][p] = pack_half2(hi[p], hi[p + 4]);
+      pl[hf][p] = pack_half2(lo[p], lo[p + 4]);
+    }
+  }
+#pragma unroll
+  for (int ks = 0; ks < 2; ++ks) {
+    *reinterpret_cast<uint4*>(dst + (0 * 2 + ks) * kXChunkBytes + lane * 16) =
+        make_uint4(ph[0][2 * ks], ph[1][2 * ks], ph[0][2 * ks + 1], ph[1][2 * ks + 1]);
+    *reinterpret_cast<uint4*>(dst + (1 * 2 + ks) * kXChunkBytes + lane * 16) =
+        make_uint4(pl[0][2 * ks], pl[1][2 * ks], pl[0][2 * ks + 1], pl[1][2 * ks + 1]);
+  }
+  if (lane == 0) *fscale = exp2i(ex - 14);
+}
+
+// As stream_groups, for 9..16 rows: acc[c][i][r] (tile c, n8-tile i, C register r).
+template <int CH, bool SWIGLU, int WN, typename L, typename RowPtr>
+__device__ __forceinline__ bool stream_groups_xa(const RowPtr& rowptr, int M,
+                                                 const CUtensorMap* tq, const CUtensorMap* ts,
+                                                 int z, int N, int q0, int nq, int slice0,
+                                                 char* base, int& seq, unsigned int* err,
+                                                 float (&acc)[CH][4][4]) {
+  static_assert(!SWIGLU || CH >= 2, "fused SwiGLU tiles pair gate and up tiles");
+  constexpr int kRing = L::kRing;
+  constexpr int kXG = 4 * kXChunkBytes;  // prepared bytes per group
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int slice = slice0 + warp;
+  const uint32_t code_s = smem_u32(base + L::kCodeOff) + warp * kRing * CH * L::kCodeTile;
+  const uint32_t scale_s = smem_u32(base + L::kScaleOff) + warp * kRing * CH * L::kScaleTile;
+  const uint32_t bar_s = smem_u32(base + L::kBarOff) + warp * kRing * 8;
+  char* xbuf = base + L::kXOff;
+  float* fsc = reinterpret_cast<float*>(base + L::kFOff);
+  constexpr int kXGroups = L::kXGroups;  // L is a Geo with NB = 4 (2 KB per group)
+  static_assert(L::kFOff - L::kXOff == L::kXGroups * kXG, "geometry must be sized for 16 rows");
+  static_assert(L::kXGroups >= 2 * WN && WN % 2 == 0, "x region must hold two chunks");
+
+  bool any;
+  out_col<CH, SWIGLU>(slice, 0, 0, N, &any);
+
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) acc[c][i][r] = 0.0f;
+
+  const int nst = (nq + 1) >> 1;
+  auto issue = [&](int s) {
+    const int u = seq + s;
+    const int st = u % kRing;
+    const uint32_t bar = bar_s + st * 8;
+    mbar_expect_tx(bar, L::kStageTx);
+    const int row = 4 * (q0 + 2 * s);
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      const int x = tile_x<CH, SWIGLU>(slice, c, N);
+      tma_load_3d(code_s + (st * CH + c) * L::kCodeTile, tq, x, row, z, bar);
+      tma_load_3d(scale_s + (st * CH + c) * L::kScaleTile, ts, x, q0 + 2 * s, z, bar);
+    }
+  };
+  if (any && lane == 0) {
+    for (int s = 0; s < kRing - 1 && s < nst; ++s) issue(s);
+  }
+
+  const int pg = nq <= kXGroups ? ((nq + 1) & ~1) : WN;
+  for (int j = warp; j < pg; j += WN) {
+    if (j < nq) {
+      float v[2][8];
+      prep_load_xa(rowptr, M, q0 + j, v);
+      prep_store_xa(v, xbuf + j * kXG, &fsc[j]);
+    }
+  }
+  __syncthreads();
+
+  bool ok = true;
+  int fail_s = 0;
+  const float zq[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  const uint32_t xbuf_s = smem_u32(xbuf) + lane * 16;
+  const uint32_t fsc_s = smem_u32(fsc);
+  const int h = lane_chunk(g);
+  const int hA = lane_chunk(2 * t), hB = lane_chunk(2 * t + 1);
+  const int nchunks = (nq + pg - 1) / pg;
+  const int sps = pg >> 1;
+  for (int pc = 0; pc < nchunks; ++pc) {
+    const int buf = pc & 1;
+    float nv[2][8];
+    const int qn = (pc + 1) * pg + warp;
+    const bool more = pc + 1 < nchunks && qn < nq;
+    if (more) prep_load_xa(rowptr, M, q0 + qn, nv);
+    const int s_end = ((pc + 1) * sps < nst) ? (pc + 1) * sps : nst;
+    if (any) {
+      for (int s = pc * sps; s < s_end; ++s) {
+        if (ok && lane == 0 && s + kRing - 1 < nst) issue(s + kRing - 1);
+        const int u = seq + s;
+        const int st = u % kRing;
+        if (ok) {
+          const bool got = mbar_wait(bar_s + st * 8, (u / kRing) & 1, kWaitLimitNs);
+          if (!__all_sync(0xffffffffu, got)) {
+            ok = false;
+            fail_s = s;
+            if (lane == 0 && err) atomicCAS(err, 0u, 8u);  // W4A16_ERR_TIMEOUT
+          }
+        }
+        if (ok) {
+#pragma unroll (kUnrollGroups)
+          for (int j = 0; j < 2; ++j) {
+            const int qi = 2 * s + j;
+            if (qi < nq) {
+              const int r = 4 * j + t;
+              const uint32_t coff = r * 128 + ((h ^ (r & 7)) << 4);
+              const int xi = buf * pg + (qi - pc * pg);
+              const float fg = lds32f(fsc_s + xi * 4);
+              const uint32_t xa = xbuf_s + xi * kXG;
+              const uint4 A0 = lds128(xa), A1 = lds128(xa + kXChunkBytes);
+              const uint4 A2 = lds128(xa + 2 * kXChunkBytes), A3 = lds128(xa + 3 * kXChunkBytes);
+              const uint32_t ah0[4] = {A0.x, A0.y, A0.z, A0.w};
+              const uint32_t ah1[4] = {A1.x, A1.y, A1.z, A1.w};
+              const uint32_t al0[4] = {A2.x, A2.y, A2.z, A2.w};
+              const uint32_t al1[4] = {A3.x, A3.y, A3.z, A3.w};
+#pragma unroll
+              for (int c = 0; c < CH; ++c) {
+                const uint4 wq = lds128(code_s + (st * CH + c) * L::kCodeTile + coff);
+                const uint32_t srow = scale_s + (st * CH + c) * L::kScaleTile + j * 128;
+                const uint4 sa = lds128(srow + hA * 16), sb = lds128(srow + hB * 16);
+                const float sA[4] = {__uint_as_float(sa.x) * fg, __uint_as_float(sa.y) * fg,
+                                     __uint_as_float(sa.z) * fg, __uint_as_float(sa.w) * fg};
+                const float sB[4] = {__uint_as_float(sb.x) * fg, __uint_as_float(sb.y) * fg,
+                                     __uint_as_float(sb.z) * fg, __uint_as_float(sb.w) * fg};
+                const uint32_t wv[4] = {wq.x, wq.y, wq.z, wq.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  uint32_t p[4];
+                  unpack_word(wv[i], p);
+                  float d[4];
+                  mma_f16_zc(d, ah0, p[0], p[1], zq);
+                  mma_f16(d, ah1, p[2], p[3]);
+                  mma_f16(d, al0, p[0], p[1]);
+                  mma_f16(d, al1, p[2], p[3]);
+                  acc[c][i][0] = fmaf(sA[i], d[0], acc[c][i][0]);
+                  acc[c][i][1] = fmaf(sB[i], d[1], acc[c][i][1]);
+                  acc[c][i][2] = fmaf(sA[i], d[2], acc[c][i][2]);
+                  acc[c][i][3] = fmaf(sB[i], d[3], acc[c][i][3]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+      }
+    }
+    if (more)
+      prep_store_xa(nv, xbuf + ((buf ^ 1) * pg + warp) * kXG, &fsc[(buf ^ 1) * pg + warp]);
+    if (nchunks > 1) __syncthreads();
+  }
+  if (any && !ok) {
+    for (int s = fail_s; s < nst && s < fail_s + kRing; ++s) {
+      const int u = seq + s;
+      (void)mbar_wait(bar_s + (u % kRing) * 8, (u / kRing) & 1, kWaitLimitNs / 16);
+    }
+  }
+  if (any) seq += nst;
+  __syncthreads();
+  return ok;
+}
+
+// Results of the 9..16-row orientation: for tile c, row half hf (row g + 8 hf) and column
+// half e (0: columns 4 h(2t) + i, 1: columns 4 h(2t + 1) + i, i = 0..3) -> 4 values.
+template <int CH>
+__device__ __forceinline__ float4 xa_result(const float (&acc)[CH][4][4], int c, int hf, int e) {
+  const int r = 2 * hf + e;
+  return make_float4(acc[c][0][r], acc[c][1][r], acc[c][2][r], acc[c][3][r]);
+}
+
+template <int CH, bool SWIGLU>
+__device__ __forceinline__ void store_direct_xa(const float (&acc)[CH][4][4], int slice, int N,
+                                                int M, float* y) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int hh[2] = {lane_chunk(2 * t), lane_chunk(2 * t + 1)};
+#pragma unroll
+  for (int hf = 0; hf < 2; ++hf) {
+    const int m = g + 8 * hf;
+    if (m >= M) continue;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      if (SWIGLU) {
+        constexpr int H = CH / 2;
+        const int I = N >> 1;
+#pragma unroll
+        for (int c = 0; c < H; ++c) {
+          const int j = 32 * H * slice + 32 * c + 4 * hh[e];
+          if (j < I)
+            *reinterpret_cast<float4*>(y + (size_t)m * I + j) =
+                swiglu4(xa_result<CH>(acc, c, hf, e), xa_result<CH>(acc, c + H, hf, e));
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int col = 32 * CH * slice + 32 * c + 4 * hh[e];
+          if (col < N)
+            *reinterpret_cast<float4*>(y + (size_t)m * N + col) = xa_result<CH>(acc, c, hf, e);
+        }
+      }
+    }
+  }
 }
 
 }  // namespace mma
