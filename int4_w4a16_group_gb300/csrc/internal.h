@@ -26,6 +26,11 @@ unsigned int* device_error_word();
 // (b0 x b1 x 1); kind 0 = packed codes (int32, 128-byte swizzle), 1 = scales (float32).
 cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t d2, uint32_t b0, uint32_t b1);
+// General form: element type, element size and swizzle given explicitly. Out-of-range box
+// elements read as zero.
+cudaError_t make_tmap_ex(CUtensorMap* out, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                         CUtensorMapSwizzle swz, const void* base, uint64_t d0, uint64_t d1,
+                         uint64_t d2, uint32_t b0, uint32_t b1);
 
 // ---- quant.cu
 cudaError_t launch_quantize(const float* W, int K, int N, int32_t* qw, float* sc, cudaStream_t s);

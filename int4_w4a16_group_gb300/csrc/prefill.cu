@@ -1,11 +1,369 @@
-// Large-M (prefill) bf16 tensor-core path: placeholder until the tcgen05 kernel lands.
+// Large-M (prefill) contraction on the 5th-generation tensor cores (tcgen05, TMEM, TMA):
+//   y[M, N] (bf16) = x[M, K] (bf16) @ bf16(dequant(qw, sc)) with float32 accumulation.
+// The pages' activations are float32 and their kernel has no large-M form; this path serves
+// batched prefill, where the op really is a dense contraction.
+//
+// Persistent CTAs (one per SM) walk 128 x 256 output tiles, M-blocks fastest (so the x tiles of
+// a weight block are reused from L2). Per 64-deep K block of a tile:
+//   * a TMA producer warp loads the x tile (128 x 64 bf16, 128-byte swizzle = the UMMA K-major
+//     canonical layout), 8 packed rows x 256 columns of codes and 2 rows of scales;
+//   * 8 dequant warps (one thread per weight column) turn each packed word (8 consecutive k of
+//     one column) into 8 bf16 values: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
+//     (128 + n_j, 128 + n_{j+4}); a bf16 FMA subtracts 136 exactly, another multiplies by the
+//     bf16 group scale; byte permutes restore k order; one 16-byte store puts them in the
+//     swizzled K-major B tile;
+//   * one thread issues 4 tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> f32) into a TMEM
+//     accumulator and commits to the stage's "empty" barrier;
+//   * 4 epilogue warps drain the finished accumulator (double-buffered, 2 x 256 TMEM columns)
+//     with tcgen05.ld, round to bf16 and store.
+// Every barrier wait is bounded; a timeout sets the device error word and the CTA winds down.
+#include <cuda_bf16.h>
+
 #include "internal.h"
+#include "mma_core.cuh"
 
 namespace w4a16 {
+namespace {
 
-cudaError_t launch_gemm_bf16(const uint16_t*, const int32_t*, const float*, uint16_t*, int, int,
-                             int, cudaStream_t) {
-  return cudaErrorNotSupported;
+using namespace mma;
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 3;
+constexpr int kEpiWarps = 4;  // warps 0..3 (TMEM lane quadrants 0..3)
+constexpr int kProdWarp = 4;
+constexpr int kMmaWarp = 5;
+constexpr int kDeqWarp0 = 6;
+constexpr int kDeqWarps = BN / 32;  // one thread per weight column
+constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;
+constexpr int kAccCols = BN;
+constexpr int kTmemCols = 2 * kAccCols;
+
+constexpr int kABytes = BM * BK * 2;
+constexpr int kBBytes = BN * BK * 2;
+constexpr int kQBytes = (BK / 8) * BN * 4;
+constexpr int kSBytes = (BK / 32) * BN * 4;
+constexpr int kAOff = 0;
+constexpr int kBOff = kAOff + kStages * kABytes;
+constexpr int kQOff = kBOff + kStages * kBBytes;
+constexpr int kSOff = kQOff + kStages * kQBytes;
+constexpr int kBarOff = kSOff + kStages * kSBytes;
+// barriers: full[S] | bready[S] | empty[S] | accfull[2] | accempty[2] | drain
+constexpr int kFull = 0, kBReady = kStages, kEmpty = 2 * kStages, kAccFull = 3 * kStages,
+              kAccEmpty = 3 * kStages + 2, kDrain = 3 * kStages + 4;
+constexpr int kNumBars = 3 * kStages + 5;
+constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
+constexpr int kSmemBytes = kMiscOff + 16;
+constexpr int kSmemAlloc = kSmemBytes + 1024;
+constexpr uint32_t kStageTx = kABytes + kQBytes + kSBytes;
+
+// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16 (10-12 = 1),
+// both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
+                            ((uint32_t)(BM >> 4) << 24);
+
+// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle: start address >> 4
+// (bits 0-13), leading offset 16 B (unused for this layout, bits 16-29), stride between 8-row
+// groups 1024 B (bits 32-45), descriptor version 1 (bits 46-47), layout SWIZZLE_128B = 2
+// (bits 61-63). Advancing K by 16 elements inside the 128-byte row adds 32 B to the start.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+__device__ __forceinline__ uint32_t lop_and_or_bf(uint32_t a, uint32_t mask) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(r) : "r"(a), "r"(mask), "r"(0x43004300u));
+  return r;
+}
+
+// One packed word (k = 8i .. 8i+7 of a column) times its bf16 scale pair -> 8 bf16 in k order.
+__device__ __forceinline__ uint4 dequant_word_bf16(uint32_t w, uint32_t s2) {
+  const uint32_t ONE = 0x3F803F80u;    // (1, 1)
+  const uint32_t M136 = 0xC308C308u;   // (-136, -136)
+  const uint32_t NEG0 = 0x80008000u;  // (-0, -0)
+  uint32_t v[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const uint32_t p = lop_and_or_bf(w >> (4 * j), 0x000F000Fu);  // (128 + n_j, 128 + n_{j+4})
+    v[j] = bf16x2_fma(bf16x2_fma(p, ONE, M136), s2, NEG0);      // (n - 8) * s, k = j, j + 4
+  }
+  uint4 o;
+  o.x = prmt(v[0], v[1], 0x5410u);  // k 0, 1
+  o.y = prmt(v[2], v[3], 0x5410u);  // k 2, 3
+  o.z = prmt(v[0], v[1], 0x7632u);  // k 4, 5
+  o.w = prmt(v[2], v[3], 0x7632u);  // k 6, 7
+  return o;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    prefill_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
+                   const __grid_constant__ CUtensorMap tms, uint16_t* __restrict__ y, int M,
+                   int N, int K, unsigned int* err) {
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* sm = align1024(smem_raw);
+  const uint32_t sb = smem_u32(sm);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  auto bar = [&](int i) { return sb + kBarOff + 8u * (uint32_t)i; };
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + kMiscOff);
+  const int mblocks = (M + BM - 1) / BM, nblocks = (N + BN - 1) / BN;
+  const int tiles = mblocks * nblocks;
+  const int kblocks = K / BK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(kFull + s), 1);
+      mbar_init(bar(kBReady + s), kDeqWarps);
+      mbar_init(bar(kEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(kAccFull + b), 1);
+      mbar_init(bar(kAccEmpty + b), kEpiWarps);
+    }
+    mbar_init(bar(kDrain), 1);
+    misc[1] = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                     sb + kMiscOff),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = misc[0];
+
+  auto fail = [&]() {
+    if (err) atomicCAS(err, 0u, 8u);  // W4A16_ERR_TIMEOUT
+    misc[1] = 1;
+  };
+  auto aborted = [&]() { return misc[1] != 0; };
+
+  if (warp == kProdWarp) {
+    if (lane == 0) {
+      int it = 0;
+      for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x) {
+        const int mb = tile % mblocks, nb = tile / mblocks;
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages, use = it / kStages;
+          if (!mbar_wait(bar(kEmpty + s), (use & 1) ^ 1, kWaitLimitNs) || aborted()) {
+            fail();
+            break;
+          }
+          mbar_expect_tx(bar(kFull + s), kStageTx);
+          tma_load_3d(sb + kAOff + s * kABytes, &tmx, kb * BK, mb * BM, 0, bar(kFull + s));
+          tma_load_3d(sb + kQOff + s * kQBytes, &tmq, nb * BN, kb * (BK / 8), 0, bar(kFull + s));
+          tma_load_3d(sb + kSOff + s * kSBytes, &tms, nb * BN, kb * (BK / 32), 0, bar(kFull + s));
+        }
+      }
+      // Let the last copies land before the CTA can exit (they target this CTA's memory).
+      for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
+        (void)mbar_wait(bar(kFull + j % kStages), (j / kStages) & 1, kWaitLimitNs / 16);
+    }
+  } else if (warp >= kDeqWarp0) {
+    const int n = (warp - kDeqWarp0) * 32 + lane;  // weight column within the tile
+    const uint32_t brow = (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x) {
+      for (int kb = 0; kb < kblocks; ++kb, ++it) {
+        const int s = it % kStages, use = it / kStages;
+        if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) || aborted()) {
+          fail();
+          break;
+        }
+        const uint32_t q = sb + kQOff + s * kQBytes + n * 4;
+        const uint32_t sc = sb + kSOff + s * kSBytes + n * 4;
+        const float s0 = lds32f(sc), s1 = lds32f(sc + BN * 4);
+        const __nv_bfloat162 h0 = __floats2bfloat162_rn(s0, s0), h1 = __floats2bfloat162_rn(s1, s1);
+        const uint32_t s2[2] = {*reinterpret_cast<const uint32_t*>(&h0),
+                                *reinterpret_cast<const uint32_t*>(&h1)};
+        const uint32_t bbase = sb + kBOff + s * kBBytes + brow;
+#pragma unroll
+        for (int i = 0; i < BK / 8; ++i) {
+          uint32_t w;
+          asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(w) : "r"(q + i * BN * 4));
+          const uint4 o = dequant_word_bf16(w, s2[i >> 2]);
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(
+                           bbase + (uint32_t)((i ^ (n & 7)) << 4)),
+                       "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
+                       : "memory");
+        }
+        fence_proxy_async();  // make the generic-proxy stores visible to the tensor cores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(kBReady + s));
+      }
+    }
+  } else if (warp == kMmaWarp) {
+    if (lane == 0) {
+      int it = 0, tcount = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < tiles && ok && !aborted(); tile += gridDim.x, ++tcount) {
+        const int b = tcount & 1, ause = tcount >> 1;
+        if (!mbar_wait(bar(kAccEmpty + b), (ause & 1) ^ 1, kWaitLimitNs)) {
+          fail();
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem + (uint32_t)(b * kAccCols);
+        for (int kb = 0; kb < kblocks; ++kb, ++it) {
+          const int s = it % kStages, use = it / kStages;
+          if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) ||
+              !mbar_wait(bar(kBReady + s), use & 1, kWaitLimitNs) || aborted()) {
+            fail();
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = sb + kAOff + s * kABytes, b0 = sb + kBOff + s * kBBytes;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk)
+            umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
+                      (kb > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(bar(kEmpty + s));  // frees the stage once these MMAs have read it
+        }
+        if (!ok) break;
+        umma_commit(bar(kAccFull + b));  // accumulator complete
+      }
+      // All MMAs issued by this thread have finished before TMEM is released.
+      umma_commit(bar(kDrain));
+      (void)mbar_wait(bar(kDrain), 0, kWaitLimitNs);
+    }
+  } else {  // epilogue warps 0..3: TMEM lanes 32*warp .. 32*warp + 31 = tile rows
+    int tcount = 0;
+    for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x, ++tcount) {
+      const int mb = tile % mblocks, nb = tile / mblocks;
+      const int b = tcount & 1, ause = tcount >> 1;
+      if (!mbar_wait(bar(kAccFull + b), ause & 1, kWaitLimitNs)) {
+        fail();
+        break;
+      }
+      tc_fence_after();
+      const int row = mb * BM + warp * 32 + lane;
+      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * kAccCols);
+#pragma unroll 1
+      for (int cc = 0; cc < BN / 32; ++cc) {
+        uint32_t r[32];
+        tmem_ld32(tbase + cc * 32, r);
+        tmem_wait_ld();
+        if (row < M) {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int col = nb * BN + cc * 32 + 8 * j;
+            if (col < N) {
+              uint32_t o[4];
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * e]),
+                                                                __uint_as_float(r[8 * j + 2 * e + 1]));
+                o[e] = *reinterpret_cast<const uint32_t*>(&hv);
+              }
+              *reinterpret_cast<uint4*>(y + (size_t)row * N + col) = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(kAccEmpty + b));
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kMmaWarp)
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
+                 "r"(kTmemCols)
+                 : "memory");
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
+                             int M, int N, int K, cudaStream_t s) {
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  static int attr_devices = 0;
+  const int bit = 1 << (di.device & 31);
+  if (!(attr_devices & bit)) {
+    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kSmemAlloc);
+    if (e != cudaSuccess) return e;
+    attr_devices |= bit;
+  }
+  CUtensorMap tmx, tmq, tms;
+  e = make_tmap_ex(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_128B, x,
+                   (uint64_t)K, (uint64_t)M, 1, BK, BM);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_ex(&tmq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, CU_TENSOR_MAP_SWIZZLE_NONE, qw,
+                   (uint64_t)N, (uint64_t)(K / 8), 1, BN, BK / 8);
+  if (e != cudaSuccess) return e;
+  e = make_tmap_ex(&tms, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, CU_TENSOR_MAP_SWIZZLE_NONE, sc,
+                   (uint64_t)N, (uint64_t)(K / kGroup), 1, BN, BK / 32);
+  if (e != cudaSuccess) return e;
+  const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const int grid = tiles < di.sm_count ? tiles : di.sm_count;
+  prefill_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tmx, tmq, tms, y, M, N, K,
+                                                     device_error_word());
+  return cudaGetLastError();
 }
 
 }  // namespace w4a16

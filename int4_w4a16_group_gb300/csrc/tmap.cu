@@ -40,7 +40,7 @@ struct CacheEntry {
   const void* ptr;
   uint64_t d0, d1, d2;
   uint32_t b0, b1;
-  int kind;
+  int dtype, swz;
   CUtensorMap map;
 };
 constexpr int kCacheSize = 8;
@@ -49,15 +49,14 @@ thread_local int t_next = 0;
 
 }  // namespace
 
-// 3-D tiled descriptor of a row-major [d2][d1][d0] tensor of 4-byte elements (d0 contiguous),
-// box (b0 x b1 x 1). kind 0: packed codes (int32, 128-byte swizzle); kind 1: scales (float32,
-// no swizzle). Out-of-range box elements read as zero.
-cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
-                      uint64_t d2, uint32_t b0, uint32_t b1) {
+// 3-D tiled descriptor of a row-major [d2][d1][d0] tensor (d0 contiguous), box (b0 x b1 x 1).
+cudaError_t make_tmap_ex(CUtensorMap* out, CUtensorMapDataType dtype, uint32_t elem_bytes,
+                         CUtensorMapSwizzle swz, const void* base, uint64_t d0, uint64_t d1,
+                         uint64_t d2, uint32_t b0, uint32_t b1) {
   for (int i = 0; i < kCacheSize; ++i) {
     const CacheEntry& c = t_cache[i];
     if (c.ptr == base && c.d0 == d0 && c.d1 == d1 && c.d2 == d2 && c.b0 == b0 && c.b1 == b1 &&
-        c.kind == kind) {
+        c.dtype == (int)dtype && c.swz == (int)swz) {
       *out = c.map;
       return cudaSuccess;
     }
@@ -65,16 +64,15 @@ cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0,
   std::call_once(g_encode_once, load_encode);
   if (!g_encode) return g_encode_status;
   const cuuint64_t dims[3] = {d0, d1, d2};
-  const cuuint64_t strides[2] = {d0 * 4, d0 * d1 * 4};
+  const cuuint64_t strides[2] = {d0 * elem_bytes, d0 * d1 * elem_bytes};
   const cuuint32_t box[3] = {b0, b1, 1};
   const cuuint32_t es[3] = {1, 1, 1};
   CUtensorMap m;
   memset(&m, 0, sizeof(m));
-  const CUresult r = g_encode(
-      &m, kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-      const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-      kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUresult r = g_encode(&m, dtype, 3, const_cast<void*>(base), dims, strides, box, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
   CacheEntry& c = t_cache[t_next];
   t_next = (t_next + 1) % kCacheSize;
@@ -84,10 +82,19 @@ cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0,
   c.d2 = d2;
   c.b0 = b0;
   c.b1 = b1;
-  c.kind = kind;
+  c.dtype = (int)dtype;
+  c.swz = (int)swz;
   c.map = m;
   *out = m;
   return cudaSuccess;
+}
+
+// kind 0: packed codes (int32, 128-byte swizzle); kind 1: scales (float32, no swizzle).
+cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
+                      uint64_t d2, uint32_t b0, uint32_t b1) {
+  return make_tmap_ex(out, kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                      4, kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, base,
+                      d0, d1, d2, b0, b1);
 }
 
 }  // namespace w4a16
