@@ -467,6 +467,56 @@ def run_reference(args, rank, world):
     }
 
 
+def profile_case(name: str):
+    """Runs one workload a few times at a size suited to an ncu capture (a few GB on the device,
+    inputs larger than L2) and prints its device times; used by the commands in profiles/."""
+    import torch
+    import int4_w4a16_group_gb300 as w4
+    import synth
+    stream = torch.cuda.current_stream()
+    out = {}
+    if name in ("gate_up", "down"):
+        if name == "gate_up":
+            K, N, fn = synth.SWIGLU["K"], 2 * synth.SWIGLU["I"], w4.w4a16_gemm_swiglu
+        else:
+            K, N, fn = synth.DOWN["K"], synth.DOWN["N"], w4.w4a16_gemm
+        (qw, sc), = _quantized_copies(w4, K, N, 1, seed=5000, outliers=(name == "down"))
+        for M in M_LIST:
+            x = synth.cuda_normal((M, K), 1.0, seed=M)
+            y = torch.empty((M, N // 2 if name == "gate_up" else N), device="cuda")
+            t = _time_launches(stream, [lambda: fn(x, qw, sc, y, stream=stream)] * 3)
+            out[f"M{M}_us"] = 1e3 * t[-1]
+    elif name == "prefill":
+        M, K, N = 2048, synth.PREFILL["K"], synth.PREFILL["N"]
+        (qw, sc), = _quantized_copies(w4, K, N, 1, seed=6000)
+        xb = synth.cuda_bf16_activations(M, K, seed=6)
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        t = _time_launches(stream, [lambda: w4.w4a16_gemm_bf16(xb, qw, sc, yb, stream=stream)] * 2)
+        out["M2048_us"] = 1e3 * t[-1]
+    elif name == "moe":
+        T, E, topk, K, I = 64, 64, 8, synth.MOE["K"], synth.MOE["I"]
+        gq = torch.empty((E, K // 8, 2 * I), dtype=torch.int32, device="cuda")
+        gs = torch.empty((E, K // 32, 2 * I), dtype=torch.float32, device="cuda")
+        dq = torch.empty((E, I // 8, K), dtype=torch.int32, device="cuda")
+        ds = torch.empty((E, I // 32, K), dtype=torch.float32, device="cuda")
+        for e in range(E):
+            a, b = synth.cuda_moe_expert_weights(e, K, I, seed=0)
+            w4.w4a16_quantize(a, gq[e], gs[e])
+            w4.w4a16_quantize(b, dq[e], ds[e])
+            del a, b
+        ids, logits = synth.routing(T, E, topk, seed=0)
+        x = synth.cuda_normal((T, K), 1.0, seed=0, stream=5)
+        idd = torch.from_numpy(ids).cuda()
+        wts = w4.w4a16_topk_softmax(torch.from_numpy(logits).cuda())
+        o = torch.empty((T, K), dtype=torch.float32, device="cuda")
+        t = _time_launches(stream, [lambda: w4.w4a16_moe_gemm(x, idd, wts, gq, gs, dq, ds, o,
+                                                              stream=stream)] * 2)
+        out["T64_E64_us"] = 1e3 * t[-1]
+    else:
+        raise SystemExit(f"unknown profile case {name}")
+    print(json.dumps({"profile_case": name, **out}), flush=True)
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -477,9 +527,16 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_COPIES,
                     help="rotating weight copies of the headline workload (L2 defeat)")
+    ap.add_argument("--profile-case", choices=["gate_up", "down", "moe", "prefill"],
+                    help="run one workload at ncu-capture size and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.profile_case:
+        import torch
+        torch.cuda.set_device(0)
+        profile_case(args.profile_case)
+        return 0
 
     if args.impl == "reference":
         rank = int(os.environ.get("RANK", "0"))
