@@ -51,6 +51,14 @@ cudaError_t device_info(DeviceInfo* out) {
         cudaSuccess)
       return e;
     d.smem_optin = (size_t)v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) !=
+        cudaSuccess)
+      return e;
+    d.smem_per_sm = (size_t)v;
+    if ((e = cudaDeviceGetAttribute(&v, cudaDevAttrReservedSharedMemoryPerBlock, dev)) !=
+        cudaSuccess)
+      return e;
+    d.smem_reserved = (size_t)v;
     g_info[dev] = d;
     g_info_valid[dev] = true;
   }

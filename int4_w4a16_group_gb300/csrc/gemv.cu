@@ -13,6 +13,7 @@
 
 #include "internal.h"
 #include "mma_core.cuh"
+#include "splitk.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -48,45 +49,6 @@ template <int NB, int CH>
 using CodesGeo = Geo<NB, CH, kWN, W4A16_CODES_RING, NB == 1 ? 12288 : 16384>;
 template <int CH>
 using ActsGeo = Geo<4, CH, kWN, W4A16_ACTS_RING, 16384>;
-
-// Split-K epilogue shared by both orientations: every CTA of the cluster has written its
-// partial tile red[4*NBR rows][kCols] (SwiGLU: kOut gate sums, then kOut up sums); rank r
-// finishes its share of the columns over all ranks in rank order.
-template <bool SWIGLU, int kCols>
-__device__ __forceinline__ void cluster_finish(cg::cluster_group& cluster, float* red, int tile,
-                                               int M, int N, float* y) {
-  constexpr int kOut = kCols / 2;
-  const int CK = (int)cluster.dim_blocks().y;
-  const int rank = (int)cluster.block_index().y;
-  cluster.sync();
-  if (SWIGLU) {
-    const int I = N >> 1;
-    const int per = kOut / CK;
-    for (int idx = threadIdx.x; idx < M * per; idx += blockDim.x) {
-      const int m = idx / per;
-      const int o = rank * per + (idx - m * per);
-      float gs = 0.0f, us = 0.0f;
-      for (int q = 0; q < CK; ++q) {
-        const float* r = cluster.map_shared_rank(red, q);
-        gs += r[m * kCols + o];
-        us += r[m * kCols + kOut + o];
-      }
-      const int out = tile * kOut + o;
-      if (out < I) y[(size_t)m * I + out] = silu_f(gs) * us;
-    }
-  } else {
-    const int per = kCols / CK;
-    for (int idx = threadIdx.x; idx < M * per; idx += blockDim.x) {
-      const int m = idx / per;
-      const int lc = rank * per + (idx - m * per);
-      float s = 0.0f;
-      for (int q = 0; q < CK; ++q) s += cluster.map_shared_rank(red, q)[m * kCols + lc];
-      const int out = tile * kCols + lc;
-      if (out < N) y[(size_t)m * N + out] = s;
-    }
-  }
-  cluster.sync();  // peers may still be reading this CTA's shared memory
-}
 
 template <int NB, int CH, bool SWIGLU>
 __global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)

@@ -14,7 +14,9 @@ struct DeviceInfo {
   int device;
   int sm_count;
   int cc_major, cc_minor;
-  size_t smem_optin;
+  size_t smem_optin;     // largest dynamic shared memory per block
+  size_t smem_per_sm;    // shared memory per SM
+  size_t smem_reserved;  // shared memory the system reserves per resident block
 };
 // Properties of the current device (cached per device id).
 cudaError_t device_info(DeviceInfo* out);
@@ -42,6 +44,7 @@ cudaError_t launch_dequantize(const int32_t* qw, const float* sc, int K, int N, 
 cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                         int N, int K, bool swiglu, cudaStream_t s);
 constexpr int kGemvMaxM = 16;
+
 
 // ---- moe.cu
 size_t moe_workspace_size(int T, int topk, int E, int K, int I);

@@ -21,6 +21,7 @@
 
 #include "internal.h"
 #include "mma_core.cuh"
+#include "tc_core.cuh"
 
 namespace w4a16 {
 namespace {
@@ -56,64 +57,8 @@ constexpr int kSmemBytes = kMiscOff + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
 constexpr uint32_t kStageTx = kABytes + kQBytes + kSBytes;
 
-// Instruction descriptor, kind::f16: D f32 (bits 4-5 = 1), A bf16 (7-9 = 1), B bf16 (10-12 = 1),
-// both K-major (bits 15, 16 = 0), N >> 3 at bits 17-22, M >> 4 at bits 24-28.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-// Shared-memory matrix descriptor of a K-major tile with 128-byte swizzle: start address >> 4
-// (bits 0-13), leading offset 16 B (unused for this layout, bits 16-29), stride between 8-row
-// groups 1024 B (bits 32-45), descriptor version 1 (bits 46-47), layout SWIZZLE_128B = 2
-// (bits 61-63). Advancing K by 16 elements inside the 128-byte row adds 32 B to the start.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
-  uint64_t d = (uint64_t)((saddr & 0x3FFFFu) >> 4);
-  d |= (uint64_t)1 << 16;
-  d |= (uint64_t)(1024 >> 4) << 32;
-  d |= (uint64_t)1 << 46;
-  d |= (uint64_t)2 << 61;
-  return d;
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                          uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
-__device__ __forceinline__ void umma_commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-      : "memory");
-}
-__device__ __forceinline__ void tc_fence_before() {
-  asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-  asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-      : "r"(taddr));
-}
-__device__ __forceinline__ void tmem_wait_ld() {
-  asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory");
-}
+// Instruction descriptor: bf16 x bf16 -> f32, M = 128, N = 256, both operands K-major.
+constexpr uint32_t kIdesc = tc::idesc_f16(true, BM, BN);
 
 __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
@@ -179,15 +124,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
-                     sb + kMiscOff),
-                 "r"(kTmemCols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    tc::tmem_alloc(sb + kMiscOff, kTmemCols);
   }
-  tc_fence_before();
+  tc::fence_before();
   __syncthreads();
-  tc_fence_after();
+  tc::fence_after();
   const uint32_t tmem = misc[0];
 
   auto fail = [&]() {
@@ -245,9 +186,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                        "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
                        : "memory");
         }
-        fence_proxy_async();  // make the generic-proxy stores visible to the tensor cores
+        tc::fence_proxy_async();  // make the generic-proxy stores visible to the tensor cores
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(kBReady + s));
+        if (lane == 0) tc::mbar_arrive(bar(kBReady + s));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -260,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail();
           break;
         }
-        tc_fence_after();
+        tc::fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(b * kAccCols);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStages, use = it / kStages;
@@ -270,19 +211,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          tc_fence_after();
+          tc::fence_after();
           const uint32_t a0 = sb + kAOff + s * kABytes, b0 = sb + kBOff + s * kBBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
-            umma_bf16(d_tmem, sw128_desc(a0 + kk * 32), sw128_desc(b0 + kk * 32), kIdesc,
-                      (kb > 0 || kk > 0) ? 1u : 0u);
-          umma_commit(bar(kEmpty + s));  // frees the stage once these MMAs have read it
+            tc::mma_ss(d_tmem, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32),
+                       kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(bar(kEmpty + s));  // frees the stage once these MMAs have read it
         }
         if (!ok) break;
-        umma_commit(bar(kAccFull + b));  // accumulator complete
+        tc::commit(bar(kAccFull + b));  // accumulator complete
       }
       // All MMAs issued by this thread have finished before TMEM is released.
-      umma_commit(bar(kDrain));
+      tc::commit(bar(kDrain));
       (void)mbar_wait(bar(kDrain), 0, kWaitLimitNs);
     }
   } else {  // epilogue warps 0..3: TMEM lanes 32*warp .. 32*warp + 31 = tile rows
@@ -294,14 +235,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         fail();
         break;
       }
-      tc_fence_after();
+      tc::fence_after();
       const int row = mb * BM + warp * 32 + lane;
       const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * kAccCols);
 #pragma unroll 1
       for (int cc = 0; cc < BN / 32; ++cc) {
         uint32_t r[32];
-        tmem_ld32(tbase + cc * 32, r);
-        tmem_wait_ld();
+        tc::tmem_ld32(tbase + cc * 32, r);
+        tc::tmem_wait_ld(r);
         if (row < M) {
 #pragma unroll
           for (int j = 0; j < 4; ++j) {
@@ -319,19 +260,16 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      tc_fence_before();
+      tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(kAccEmpty + b));
+      if (lane == 0) tc::mbar_arrive(bar(kAccEmpty + b));
     }
   }
 
-  tc_fence_before();
+  tc::fence_before();
   __syncthreads();
-  tc_fence_after();
-  if (warp == kMmaWarp)
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem),
-                 "r"(kTmemCols)
-                 : "memory");
+  tc::fence_after();
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
