@@ -7,8 +7,8 @@
 // a weight block are reused from L2). Per 64-deep K block of a tile:
 //   * a TMA producer warp loads the x tile (128 x 64 bf16, 128-byte swizzle = the UMMA K-major
 //     canonical layout), 8 packed rows x 256 columns of codes and 2 rows of scales;
-//   * 8 dequant warps (one thread per weight column) turn each packed word (8 consecutive k of
-//     one column) into 8 bf16 values: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
+//   * 16 dequant warps (two threads per weight column, one per group of the k-block) turn each
+//     packed word (8 consecutive k of one column) into 8 bf16 values: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
 //     (128 + n_j, 128 + n_{j+4}); a bf16 FMA subtracts 136 exactly, another multiplies by the
 //     bf16 group scale; byte permutes restore k order; one 16-byte store puts them in the
 //     swizzled K-major B tile;
@@ -34,7 +34,12 @@ constexpr int kEpiWarps = 4;  // warps 0..3 (TMEM lane quadrants 0..3)
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDeqWarp0 = 6;
-constexpr int kDeqWarps = BN / 32;  // one thread per weight column
+#ifndef W4A16_PREFILL_DEQ_SPLIT
+#define W4A16_PREFILL_DEQ_SPLIT 2
+#endif
+constexpr int kDeqSplit = W4A16_PREFILL_DEQ_SPLIT;  // threads per weight column (groups per k-block split)
+static_assert(kDeqSplit == 1 || kDeqSplit == 2, "a 64-deep k-block holds two groups");
+constexpr int kDeqWarps = kDeqSplit * BN / 32;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;
 constexpr int kAccCols = BN;
 constexpr int kTmemCols = 2 * kAccCols;
@@ -159,7 +164,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         (void)mbar_wait(bar(kFull + j % kStages), (j / kStages) & 1, kWaitLimitNs / 16);
     }
   } else if (warp >= kDeqWarp0) {
-    const int n = (warp - kDeqWarp0) * 32 + lane;  // weight column within the tile
+    // Thread = weight column n of the tile and, with two threads per column, group h of the
+    // 64-deep k-block (words 4h .. 4h + 3).
+    constexpr int kWords = (BK / 8) / kDeqSplit;
+    const int n = ((warp - kDeqWarp0) % (BN / 32)) * 32 + lane;
+    const int h = (warp - kDeqWarp0) / (BN / 32);
     const uint32_t brow = (uint32_t)(n >> 3) * 1024u + (uint32_t)(n & 7) * 128u;
     int it = 0;
     for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x) {
@@ -169,18 +178,24 @@ __global__ void __launch_bounds__(kThreads, 1)
           fail();
           break;
         }
-        const uint32_t q = sb + kQOff + s * kQBytes + n * 4;
+        const uint32_t q = sb + kQOff + s * kQBytes + (h * kWords * BN + n) * 4;
         const uint32_t sc = sb + kSOff + s * kSBytes + n * 4;
-        const float s0 = lds32f(sc), s1 = lds32f(sc + BN * 4);
-        const __nv_bfloat162 h0 = __floats2bfloat162_rn(s0, s0), h1 = __floats2bfloat162_rn(s1, s1);
-        const uint32_t s2[2] = {*reinterpret_cast<const uint32_t*>(&h0),
-                                *reinterpret_cast<const uint32_t*>(&h1)};
+        // bf16 scale pair of each group this thread covers (group g of the k-block = words
+        // 4g .. 4g + 3).
+        uint32_t s2[2];
+#pragma unroll
+        for (int gq = 0; gq < 2 / kDeqSplit; ++gq) {
+          const float sv = lds32f(sc + (h * (2 / kDeqSplit) + gq) * BN * 4);
+          const __nv_bfloat162 hv = __floats2bfloat162_rn(sv, sv);
+          s2[gq] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
         const uint32_t bbase = sb + kBOff + s * kBBytes + brow;
 #pragma unroll
-        for (int i = 0; i < BK / 8; ++i) {
+        for (int ii = 0; ii < kWords; ++ii) {
+          const int i = h * kWords + ii;  // word (8 consecutive k) within the k-block
           uint32_t w;
-          asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(w) : "r"(q + i * BN * 4));
-          const uint4 o = dequant_word_bf16(w, s2[i >> 2]);
+          asm volatile("ld.shared.b32 %0, [%1];\n" : "=r"(w) : "r"(q + ii * BN * 4));
+          const uint4 o = dequant_word_bf16(w, s2[ii >> 2]);
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(
                            bbase + (uint32_t)((i ^ (n & 7)) << 4)),
                        "r"(o.x), "r"(o.y), "r"(o.z), "r"(o.w)
