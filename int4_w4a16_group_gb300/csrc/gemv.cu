@@ -249,12 +249,24 @@ cudaError_t launch_acts(const float* x, const int32_t* qw, const float* sc, floa
                       y, M, N, K, di, s);
 }
 
-// Up to 4 rows: 4 tiles per warp (128 columns) when the problem is wide enough to give every
-// SM several warps, else 2; 5..8 rows: 2; 9..16 rows: the activations-as-A kernel, 2 tiles.
+// CTAs a problem can occupy with CH tiles per warp: column tiles times the largest split that
+// still leaves each CTA 8 groups of K (at most a 16-CTA cluster).
+template <int CH, bool SWIGLU>
+long long fill_of(int N, int K) {
+  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
+  int ck = 1;
+  while (ck < kMaxCluster && (K / kGroup) / (2 * ck) >= 8) ck *= 2;
+  return (long long)tiles * ck;
+}
+
+// Up to 4 rows: 4 tiles per warp (128 columns) when that still fills the GPU with CTAs (4 per
+// SM), else 2; 5..8 rows: 2; 9..16 rows: the activations-as-A kernel, 2 tiles.
 template <bool SWIGLU>
 cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
                      int K, const DeviceInfo& di, cudaStream_t s) {
-  const bool wide = slices_of<4, SWIGLU>(N) * 8 >= 2 * di.sm_count;
+  const long long slots = 4LL * di.sm_count;
+  const bool wide = fill_of<W4A16_WIDE_CH, SWIGLU>(N, K) * 10 >= slots * 8 ||
+                    fill_of<W4A16_WIDE_CH, SWIGLU>(N, K) >= fill_of<2, SWIGLU>(N, K);
   if (M <= 4)
     return wide ? launch_codes<1, W4A16_WIDE_CH, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
                 : launch_codes<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
