@@ -6,7 +6,8 @@
 // Persistent CTAs (one per SM) walk 128 x 256 output tiles, M-blocks fastest (so the x tiles of
 // a weight block are reused from L2). Per 64-deep K block of a tile:
 //   * a TMA producer warp loads the x tile (128 x 64 bf16, 128-byte swizzle = the UMMA K-major
-//     canonical layout), 8 packed rows x 256 columns of codes and 2 rows of scales;
+//     canonical layout), 8 packed rows x 256 columns of codes and 2 rows of scales into a ring
+//     of its own (the B tiles below have a separate, shorter ring);
 //   * 16 dequant warps (two threads per weight column, one per group of the k-block) turn each
 //     packed word (8 consecutive k of one column) into 8 bf16 values: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
 //     (128 + n_j, 128 + n_{j+4}); a bf16 FMA subtracts 136 exactly, another multiplies by the
@@ -29,7 +30,16 @@ namespace {
 using namespace mma;
 
 constexpr int BM = 128, BN = 256, BK = 64;
-constexpr int kStages = 3;
+// Two rings: the TMA ring of x tiles, codes and scales (kStagesA), and the ring of dequantized
+// bf16 B tiles (kStagesB), so TMA can run further ahead than the dequant warps need B tiles.
+#ifndef W4A16_PREFILL_STAGES_A
+#define W4A16_PREFILL_STAGES_A 5
+#endif
+#ifndef W4A16_PREFILL_STAGES_B
+#define W4A16_PREFILL_STAGES_B 2
+#endif
+constexpr int kStagesA = W4A16_PREFILL_STAGES_A;
+constexpr int kStagesB = W4A16_PREFILL_STAGES_B;
 constexpr int kEpiWarps = 4;  // warps 0..3 (TMEM lane quadrants 0..3)
 constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
@@ -49,14 +59,16 @@ constexpr int kBBytes = BN * BK * 2;
 constexpr int kQBytes = (BK / 8) * BN * 4;
 constexpr int kSBytes = (BK / 32) * BN * 4;
 constexpr int kAOff = 0;
-constexpr int kBOff = kAOff + kStages * kABytes;
-constexpr int kQOff = kBOff + kStages * kBBytes;
-constexpr int kSOff = kQOff + kStages * kQBytes;
-constexpr int kBarOff = kSOff + kStages * kSBytes;
-// barriers: full[S] | bready[S] | empty[S] | accfull[2] | accempty[2] | drain
-constexpr int kFull = 0, kBReady = kStages, kEmpty = 2 * kStages, kAccFull = 3 * kStages,
-              kAccEmpty = 3 * kStages + 2, kDrain = 3 * kStages + 4;
-constexpr int kNumBars = 3 * kStages + 5;
+constexpr int kQOff = kAOff + kStagesA * kABytes;
+constexpr int kSOff = kQOff + kStagesA * kQBytes;
+constexpr int kBOff = kSOff + kStagesA * kSBytes;  // 1024-aligned: SW128 tiles
+constexpr int kBarOff = kBOff + kStagesB * kBBytes;
+static_assert(kBOff % 1024 == 0, "B tiles need 1024-byte alignment");
+// barriers: full[SA] | empty[SA] | bready[SB] | bempty[SB] | accfull[2] | accempty[2] | drain
+constexpr int kFull = 0, kEmpty = kStagesA, kBReady = 2 * kStagesA,
+              kBEmpty = 2 * kStagesA + kStagesB, kAccFull = 2 * kStagesA + 2 * kStagesB,
+              kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2;
+constexpr int kNumBars = kDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
 constexpr int kSmemBytes = kMiscOff + 16;
 constexpr int kSmemAlloc = kSmemBytes + 1024;
@@ -115,10 +127,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int kblocks = K / BK;
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kStagesA; ++s) {
       mbar_init(bar(kFull + s), 1);
-      mbar_init(bar(kBReady + s), kDeqWarps);
       mbar_init(bar(kEmpty + s), 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(bar(kBReady + s), kDeqWarps);
+      mbar_init(bar(kBEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(kAccFull + b), 1);
@@ -148,7 +163,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x) {
         const int mb = tile % mblocks, nb = tile / mblocks;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % kStages, use = it / kStages;
+          const int s = it % kStagesA, use = it / kStagesA;
           if (!mbar_wait(bar(kEmpty + s), (use & 1) ^ 1, kWaitLimitNs) || aborted()) {
             fail();
             break;
@@ -160,8 +175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       // Let the last copies land before the CTA can exit (they target this CTA's memory).
-      for (int j = (it > kStages ? it - kStages : 0); j < it; ++j)
-        (void)mbar_wait(bar(kFull + j % kStages), (j / kStages) & 1, kWaitLimitNs / 16);
+      for (int j = (it > kStagesA ? it - kStagesA : 0); j < it; ++j)
+        (void)mbar_wait(bar(kFull + j % kStagesA), (j / kStagesA) & 1, kWaitLimitNs / 16);
     }
   } else if (warp >= kDeqWarp0) {
     // Thread = weight column n of the tile and, with two threads per column, group h of the
@@ -173,8 +188,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x) {
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
-        const int s = it % kStages, use = it / kStages;
-        if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) || aborted()) {
+        const int s = it % kStagesA, use = it / kStagesA;
+        const int sbt = it % kStagesB, useb = it / kStagesB;
+        if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) ||
+            !mbar_wait(bar(kBEmpty + sbt), (useb & 1) ^ 1, kWaitLimitNs) || aborted()) {
           fail();
           break;
         }
@@ -189,7 +206,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const __nv_bfloat162 hv = __floats2bfloat162_rn(sv, sv);
           s2[gq] = *reinterpret_cast<const uint32_t*>(&hv);
         }
-        const uint32_t bbase = sb + kBOff + s * kBBytes + brow;
+        const uint32_t bbase = sb + kBOff + sbt * kBBytes + brow;
 #pragma unroll
         for (int ii = 0; ii < kWords; ++ii) {
           const int i = h * kWords + ii;  // word (8 consecutive k) within the k-block
@@ -203,7 +220,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_proxy_async();  // make the generic-proxy stores visible to the tensor cores
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(kBReady + s));
+        if (lane == 0) tc::mbar_arrive(bar(kBReady + sbt));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -219,20 +236,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_after();
         const uint32_t d_tmem = tmem + (uint32_t)(b * kAccCols);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
-          const int s = it % kStages, use = it / kStages;
+          const int s = it % kStagesA, use = it / kStagesA;
+          const int sbt = it % kStagesB, useb = it / kStagesB;
           if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) ||
-              !mbar_wait(bar(kBReady + s), use & 1, kWaitLimitNs) || aborted()) {
+              !mbar_wait(bar(kBReady + sbt), useb & 1, kWaitLimitNs) || aborted()) {
             fail();
             ok = false;
             break;
           }
           tc::fence_after();
-          const uint32_t a0 = sb + kAOff + s * kABytes, b0 = sb + kBOff + s * kBBytes;
+          const uint32_t a0 = sb + kAOff + s * kABytes, b0 = sb + kBOff + sbt * kBBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_ss(d_tmem, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32),
                        kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(bar(kEmpty + s));  // frees the stage once these MMAs have read it
+          tc::commit(bar(kEmpty + s));     // frees the x/codes stage once these MMAs read it
+          tc::commit(bar(kBEmpty + sbt));  // and the B tile
         }
         if (!ok) break;
         tc::commit(bar(kAccFull + b));  // accumulator complete
