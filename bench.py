@@ -200,6 +200,20 @@ def _time_launches(stream, fns):
     return [ev[i].elapsed_time(ev[i + 1]) for i in range(len(fns))]
 
 
+def _time_region(stream, fns):
+    """Runs fns in order on `stream` with events only around the whole sequence (so consecutive
+    kernels may overlap their launch and prologue as they do in a real step); returns ms."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(20e6))
+    a.record(stream)
+    for fn in fns:
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b)
+
+
 def run_ours(args, rank, world):
     import torch
     import int4_w4a16_group_gb300 as w4
@@ -239,18 +253,22 @@ def run_ours(args, rank, world):
         fns = []
         for _ in range(args.steps):
             fns.extend(step_fns())
-        times = _time_launches(stream, fns)
+        total_ms = _time_region(stream, fns)
         barrier(world)
         torch.cuda.synchronize()
     clocks = clk.summary()
-    total_ms = sum(times)
+    # per-M breakdown: a second pass with an event after every launch
+    fns = []
+    for _ in range(args.steps):
+        fns.extend(step_fns())
+    times = _time_launches(stream, fns)
     for i, t in enumerate(times):
         per_launch[M_LIST[i % len(M_LIST)]].append(t)
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
     value = world * args.steps * len(M_LIST) * wbytes / (total_ms * 1e-3) / 1e9
 
-    avg_launch_ms = sum(times) / len(times)
+    avg_launch_ms = total_ms / (args.steps * len(M_LIST))
     achieved = wbytes / (avg_launch_ms * 1e-3) / 1e9
     per_m = {str(M): {"us": 1e3 * statistics.mean(per_launch[M]),
                       "GB/s": wbytes / (statistics.mean(per_launch[M]) * 1e-3) / 1e9,
@@ -380,6 +398,23 @@ def other_workloads(args, w4, peaks, stream):
                                              "frac_of_bf16": tf / peaks["bf16_tflops"]}
     except Exception as ex:  # the bf16 kernel may be unavailable in this build
         res["prefill_M4096_K7168_N18432"] = {"unavailable": str(ex).splitlines()[0]}
+
+    # bf16 activations at small M (K=7168, N=18432, bf16 in and out), 4 rotating weight copies
+    K, N = synth.PREFILL["K"], synth.PREFILL["N"]
+    wb = BYTES_PER_WEIGHT * K * N
+    copies = _quantized_copies(w4, K, N, N_COPIES, seed=5000)
+    b16 = {}
+    for M in M_LIST:
+        xb = synth.cuda_bf16_activations(M, K, seed=8 + M)
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        fns = [lambda c=c: w4.w4a16_gemm_bf16(xb, copies[c % N_COPIES][0], copies[c % N_COPIES][1],
+                                              yb, stream=stream) for c in range(reps + 3)]
+        t = _time_launches(stream, fns)[3:]
+        us = 1e3 * statistics.mean(t)
+        b16[str(M)] = {"us": us, "GB/s": wb / (us * 1e-6) / 1e9,
+                       "frac_of_hbm": wb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    res["bf16_small_M_K7168_N18432"] = b16
+    del copies
 
     # tiny: launch-latency bound
     c = synth.TINY

@@ -98,10 +98,12 @@ w4a16_status w4a16_gemm_swiglu(const float* x, const int32_t* qw_gu, const float
                                float* y, int M, int N2, int K, int group,
                                w4a16_stream_t stream);
 
-/* Large-M (prefill) contraction on the tensor cores: bf16 activations x[M, K] (bit patterns),
- * dequantized weights rounded to bf16, float32 accumulation, bf16 output y[M, N].
- * Not on the pages (their activations are float32); tolerance 1e-2 relative L2 against the
- * exact product. Needs an sm_103 device; K % 64 == 0 and N % 8 == 0. */
+/* GEMM with bf16 activations x[M, K] (bit patterns) and bf16 output y[M, N], float32
+ * accumulation. M > 16 (prefill) runs the tensor-core contraction with the dequantized weights
+ * rounded to bf16; M <= 16 runs the weight-streaming kernels in bf16 form (exact codes, scale
+ * applied in float32 per group). Not on the pages (their activations are float32); tolerance
+ * 1e-2 relative L2 against the exact product. Needs an sm_103 device; K % 64 == 0, N % 8 == 0,
+ * x and y 16-byte aligned. Deterministic. */
 w4a16_status w4a16_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* sc,
                              uint16_t* y, int M, int N, int K, int group,
                              w4a16_stream_t stream);

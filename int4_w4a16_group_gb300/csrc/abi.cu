@@ -196,7 +196,10 @@ w4a16_status w4a16_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* 
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return cuda_status(e);
   if (di.cc_major != 10 || di.cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
-  e = launch_gemm_bf16(x, qw, sc, y, M, N, K, (cudaStream_t)stream);
+  // Up to 16 rows the op is weight streaming: the small-M kernels (bf16 form) read each packed
+  // weight once; larger M is the tensor-core contraction.
+  e = M <= kGemvMaxM ? launch_gemv_b16(x, qw, sc, y, M, N, K, (cudaStream_t)stream)
+                     : launch_gemm_bf16(x, qw, sc, y, M, N, K, (cudaStream_t)stream);
   if (e == cudaErrorNotSupported) return W4A16_ERR_UNSUPPORTED;
   return cuda_status(e);
 }

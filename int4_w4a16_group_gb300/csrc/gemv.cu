@@ -10,6 +10,7 @@
 // distributed shared memory in rank order: deterministic, no global scratch, no atomics.
 // The per-warp main loop lives in mma_core.cuh.
 #include <cooperative_groups.h>
+#include <cuda_bf16.h>
 
 #include "internal.h"
 #include "mma_core.cuh"
@@ -43,6 +44,9 @@ constexpr int kWN = 4;  // warps (slices) per CTA
 #endif
 #ifndef W4A16_WIDE_CH
 #define W4A16_WIDE_CH 4
+#endif
+#ifndef W4A16_B16_WIDE_CH
+#define W4A16_B16_WIDE_CH 4
 #endif
 
 template <int NB, int CH>
@@ -145,6 +149,79 @@ __global__ void __launch_bounds__(kWN * 32, W4A16_ACTS_MINB)
   cluster_finish<SWIGLU, kCols>(cluster, red, tile, M, N, y);
 }
 
+// bf16 activations (x[M, K] bf16, y[M, N] bf16, M <= 16): the codes orientation with x rows as
+// MMA columns, 8 rows per n8 block. Lane (g, t) ends with rows 8b + 2t and 8b + 2t + 1 of n8 block
+// b; for each of them the lane's 4 columns 4 h(g) + 0..3 of tile c are below.
+template <int NB, int CH>
+__device__ __forceinline__ float4 b16_result(const float (&acc)[CH][2][NB][4], int c, int b,
+                                             int odd) {
+  return make_float4(acc[c][0][b][odd], acc[c][0][b][2 + odd], acc[c][1][b][odd],
+                     acc[c][1][b][2 + odd]);
+}
+
+template <int NB, int CH>
+__global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
+    gemv_b16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
+                    const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int M, int N, int K,
+                    unsigned int* err) {
+  using L = CodesGeo<NB, CH>;
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* smem = align1024(smem_raw);
+  cg::cluster_group cluster = cg::this_cluster();
+  const int tile = blockIdx.x;
+  const int CK = (int)cluster.dim_blocks().y;
+  const int rank = (int)cluster.block_index().y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int G = K / kGroup;
+  const int q0 = (int)((long long)rank * G / CK);
+  const int q1 = (int)((long long)(rank + 1) * G / CK);
+
+  init_barriers<L>(smem, kWN);
+  float acc[CH][2][NB][4];
+  int seq = 0;
+  auto rowptr = [&](int m) { return x + (size_t)m * K; };
+  stream_groups<NB, CH, false, kWN, L, true>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN,
+                                             smem, seq, err, acc);
+  if (CK == 1) {
+#pragma unroll
+    for (int c = 0; c < CH; ++c) {
+      bool valid;
+      const int col = out_col<CH, false>(tile * kWN + warp, c, g, N, &valid);
+      if (!valid) continue;
+#pragma unroll
+      for (int b = 0; b < NB; ++b)
+#pragma unroll
+        for (int odd = 0; odd < 2; ++odd) {
+          const int m = 8 * b + 2 * t + odd;
+          if (m < M) {
+            const float4 v = b16_result<NB, CH>(acc, c, b, odd);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+            uint2 o;
+            o.x = *reinterpret_cast<const uint32_t*>(&lo);
+            o.y = *reinterpret_cast<const uint32_t*>(&hi);
+            *reinterpret_cast<uint2*>(y + (size_t)m * N + col) = o;
+          }
+        }
+    }
+    return;
+  }
+  constexpr int kCols = kWN * 32 * CH;
+  static_assert(8 * NB * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
+                "split-K tile must fit in the code ring");
+  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
+#pragma unroll
+  for (int c = 0; c < CH; ++c)
+#pragma unroll
+    for (int b = 0; b < NB; ++b)
+#pragma unroll
+      for (int odd = 0; odd < 2; ++odd)
+        *reinterpret_cast<float4*>(&red[(8 * b + 2 * t + odd) * kCols +
+                                        tile_local_col<CH, false, kWN>(warp, c, g)]) =
+            b16_result<NB, CH>(acc, c, b, odd);
+  cluster_finish<false, kCols, uint16_t>(cluster, red, tile, M, N, y);
+}
+
 constexpr int kMaxCluster = 16;
 
 struct LaunchCache {
@@ -161,9 +238,9 @@ int slices_of(int N) {
 
 // Launches `kern` over tiles x CK clusters, CK chosen so that the waves of clusters fill the GPU
 // most evenly (each CTA keeps at least 8 groups of K).
-template <typename Kern>
-cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, const float* x,
-                         const int32_t* qw, const float* sc, float* y, int M, int N, int K,
+template <typename Kern, typename XT, typename YT>
+cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, const XT* x,
+                         const int32_t* qw, const float* sc, YT* y, int M, int N, int K,
                          const DeviceInfo& di, cudaStream_t s) {
   const int G = K / kGroup;
   const int bit = 1 << (di.device & 31);
@@ -275,7 +352,31 @@ cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* 
   return cudaErrorInvalidValue;
 }
 
+template <int NB, int CH>
+cudaError_t launch_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y, int M,
+                       int N, int K, const DeviceInfo& di, cudaStream_t s) {
+  static LaunchCache cache;
+  const int tiles = (slices_of<CH, false>(N) + kWN - 1) / kWN;
+  return launch_split(gemv_b16_kernel<NB, CH>, CodesGeo<NB, CH>::kAlloc, cache, tiles, x, qw, sc,
+                      y, M, N, K, di, s);
+}
+
 }  // namespace
+
+cudaError_t launch_gemv_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
+                            int M, int N, int K, cudaStream_t s) {
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  const long long slots = 4LL * di.sm_count;
+  const bool wide = fill_of<W4A16_B16_WIDE_CH, false>(N, K) * 10 >= slots * 8 ||
+                    fill_of<W4A16_B16_WIDE_CH, false>(N, K) >= fill_of<2, false>(N, K);
+  if (M <= 8)
+    return wide ? launch_b16<1, W4A16_B16_WIDE_CH>(x, qw, sc, y, M, N, K, di, s)
+                : launch_b16<1, 2>(x, qw, sc, y, M, N, K, di, s);
+  if (M <= 16) return launch_b16<2, 2>(x, qw, sc, y, M, N, K, di, s);
+  return cudaErrorInvalidValue;
+}
 
 cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                         int N, int K, bool swiglu, cudaStream_t s) {

@@ -174,6 +174,48 @@ __device__ __forceinline__ void unpack_pair(uint32_t wa, uint32_t wb, uint32_t (
   a1[3] = hfma2_u32(lop_and_or(wb8, 0x00F000F0u), SIXTEENTH, M72);
 }
 
+// bf16 forms for activations that arrive in bf16: A and B of one MMA share their type, so the
+// codes are unpacked to bf16 instead. ((w >> 4j) & 0x000F000F) | 0x43004300 is the bf16 pair
+// (128 + n_j, 128 + n_{j+4}); one bf16 FMA subtracts 136 exactly. Same register order as
+// unpack_pair.
+__device__ __forceinline__ uint32_t bfma2_u32(uint32_t a, uint32_t b, uint32_t c) {
+  uint32_t r;
+  asm("fma.rn.bf16x2 %0, %1, %2, %3;\n" : "=r"(r) : "r"(a), "r"(b), "r"(c));
+  return r;
+}
+__device__ __forceinline__ uint32_t lop_and_or_b16(uint32_t a) {
+  uint32_t r;
+  asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(r) : "r"(a), "r"(0x000F000Fu), "r"(0x43004300u));
+  return r;
+}
+__device__ __forceinline__ void unpack_pair_b16(uint32_t wa, uint32_t wb, uint32_t (&a0)[4],
+                                                uint32_t (&a1)[4]) {
+  const uint32_t ONE = 0x3F803F80u, M136 = 0xC308C308u;  // bf16 (1, 1), (-136, -136)
+  a0[0] = bfma2_u32(lop_and_or_b16(wa), ONE, M136);
+  a0[1] = bfma2_u32(lop_and_or_b16(wb), ONE, M136);
+  a0[2] = bfma2_u32(lop_and_or_b16(wa >> 4), ONE, M136);
+  a0[3] = bfma2_u32(lop_and_or_b16(wb >> 4), ONE, M136);
+  a1[0] = bfma2_u32(lop_and_or_b16(wa >> 8), ONE, M136);
+  a1[1] = bfma2_u32(lop_and_or_b16(wb >> 8), ONE, M136);
+  a1[2] = bfma2_u32(lop_and_or_b16(wa >> 12), ONE, M136);
+  a1[3] = bfma2_u32(lop_and_or_b16(wb >> 12), ONE, M136);
+}
+__device__ __forceinline__ void mma_b16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                        uint32_t b1) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_b16_zc(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                           uint32_t b1, const float (&z)[4]) {
+  asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%10,%11,%12,%13};\n"
+      : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1), "f"(z[0]), "f"(z[1]),
+        "f"(z[2]), "f"(z[3]));
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float lo, float hi) {
   const __half2 h = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<const uint32_t*>(&h);
@@ -247,6 +289,58 @@ __device__ __forceinline__ void prep_store(const float (&v)[NB][8], char* dst, f
     *reinterpret_cast<uint4*>(dst + b * kXChunkBytes + lane * 16) = r;
   }
   if (lane == 0) *fscale = exp2i(ex - 14);
+}
+
+// Activations in bf16: no split is needed (an MMA column is one row m = 8b + g of x, the
+// product of a bf16 activation and an exact code is exact in fp32) and no exponent (fscale = 1).
+// prep_load_b16: lane (g, t) loads x[m][32q + 8t .. +7] (16 bytes) for m = 8b + g;
+// prep_store_b16: byte permutes put the 8 values in the k order of the codes
+// (0, 4, 1, 5, 2, 6, 3, 7) and write NB x 512 B at dst.
+template <int NB, bool B16>
+struct PrepRegs {
+  float v[NB][8];
+};
+template <int NB>
+struct PrepRegs<NB, true> {
+  uint4 v[NB];
+};
+
+template <int NB, typename RowPtr>
+__device__ __forceinline__ void prep_load_b16(const RowPtr& rowptr, int M, int q, uint4 (&v)[NB]) {
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    const int m = 8 * b + g;
+    v[b] = m < M ? __ldg(reinterpret_cast<const uint4*>(rowptr(m) + 32 * q + 8 * t))
+                 : make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+template <int NB>
+__device__ __forceinline__ void prep_store_b16(const uint4 (&v)[NB], char* dst, float* fscale) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int b = 0; b < NB; ++b) {
+    uint4 r;
+    r.x = __byte_perm(v[b].x, v[b].z, 0x5410);  // k 0, 4
+    r.y = __byte_perm(v[b].x, v[b].z, 0x7632);  // k 1, 5
+    r.z = __byte_perm(v[b].y, v[b].w, 0x5410);  // k 2, 6
+    r.w = __byte_perm(v[b].y, v[b].w, 0x7632);  // k 3, 7
+    *reinterpret_cast<uint4*>(dst + b * kXChunkBytes + lane * 16) = r;
+  }
+  if (lane == 0) *fscale = 1.0f;
+}
+
+template <int NB, bool B16, typename RowPtr>
+__device__ __forceinline__ void prep_load_any(const RowPtr& rowptr, int M, int q,
+                                              PrepRegs<NB, B16>& r) {
+  if constexpr (B16) prep_load_b16<NB>(rowptr, M, q, r.v);
+  else prep_load<NB>(rowptr, M, q, r.v);
+}
+template <int NB, bool B16>
+__device__ __forceinline__ void prep_store_any(const PrepRegs<NB, B16>& r, char* dst,
+                                               float* fscale) {
+  if constexpr (B16) prep_store_b16<NB>(r.v, dst, fscale);
+  else prep_store<NB>(r.v, dst, fscale);
 }
 
 // ------------------------------------------------------------------------------ geometry
@@ -342,7 +436,7 @@ __device__ __forceinline__ void init_barriers(char* base, int warps) {
 // C register r). `seq` counts the stages this warp has used so far (barrier phases carry on
 // across calls). Returns false if a barrier wait gave up (the error word is then set).
 // All threads of the CTA must call this (it synchronizes the CTA around the x fragments).
-template <int NB, int CH, bool SWIGLU, int WN, typename L, typename RowPtr>
+template <int NB, int CH, bool SWIGLU, int WN, typename L, bool B16 = false, typename RowPtr>
 __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
                                               const CUtensorMap* tq, const CUtensorMap* ts,
                                               int z, int N, int q0, int nq, int slice0,
@@ -396,9 +490,9 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
   const int pg = nq <= L::kXGroups ? ((nq + 1) & ~1) : WN;
   for (int j = warp; j < pg; j += WN) {
     if (j < nq) {
-      float v[NB][8];
-      prep_load<NB>(rowptr, M, q0 + j, v);
-      prep_store<NB>(v, xbuf + j * NB * kXChunkBytes, &fsc[j]);
+      PrepRegs<NB, B16> v;
+      prep_load_any<NB, B16>(rowptr, M, q0 + j, v);
+      prep_store_any<NB, B16>(v, xbuf + j * NB * kXChunkBytes, &fsc[j]);
     }
   }
   __syncthreads();
@@ -414,10 +508,10 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
   for (int pc = 0; pc < nchunks; ++pc) {
     const int buf = pc & 1;
     // Next chunk's activations: loads now, conversion after this chunk's compute.
-    float nv[NB][8];
+    PrepRegs<NB, B16> nv;
     const int qn = (pc + 1) * pg + warp;
     const bool more = pc + 1 < nchunks && qn < nq;
-    if (more) prep_load<NB>(rowptr, M, q0 + qn, nv);
+    if (more) prep_load_any<NB, B16>(rowptr, M, q0 + qn, nv);
     const int s_end = ((pc + 1) * sps < nst) ? (pc + 1) * sps : nst;
     if (any) {
       for (int s = pc * sps; s < s_end; ++s) {
@@ -460,12 +554,20 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
 #pragma unroll
                 for (int T = 0; T < 2; ++T) {
                   uint32_t a0[4], a1[4];
-                  unpack_pair(T ? wq[c].z : wq[c].x, T ? wq[c].w : wq[c].y, a0, a1);
+                  if constexpr (B16)
+                    unpack_pair_b16(T ? wq[c].z : wq[c].x, T ? wq[c].w : wq[c].y, a0, a1);
+                  else
+                    unpack_pair(T ? wq[c].z : wq[c].x, T ? wq[c].w : wq[c].y, a0, a1);
 #pragma unroll
                   for (int b = 0; b < NB; ++b) {
                     float d[4];
-                    mma_f16_zc(d, a0, bf[b].x, bf[b].y, zq);
-                    mma_f16(d, a1, bf[b].z, bf[b].w);
+                    if constexpr (B16) {
+                      mma_b16_zc(d, a0, bf[b].x, bf[b].y, zq);
+                      mma_b16(d, a1, bf[b].z, bf[b].w);
+                    } else {
+                      mma_f16_zc(d, a0, bf[b].x, bf[b].y, zq);
+                      mma_f16(d, a1, bf[b].z, bf[b].w);
+                    }
                     acc[c][T][b][0] = fmaf(sv[2 * T], d[0], acc[c][T][b][0]);
                     acc[c][T][b][1] = fmaf(sv[2 * T], d[1], acc[c][T][b][1]);
                     acc[c][T][b][2] = fmaf(sv[2 * T + 1], d[2], acc[c][T][b][2]);
@@ -480,8 +582,8 @@ __device__ __forceinline__ bool stream_groups(const RowPtr& rowptr, int M,
       }
     }
     if (more)
-      prep_store<NB>(nv, xbuf + ((buf ^ 1) * pg + warp) * NB * kXChunkBytes,
-                     &fsc[(buf ^ 1) * pg + warp]);
+      prep_store_any<NB, B16>(nv, xbuf + ((buf ^ 1) * pg + warp) * NB * kXChunkBytes,
+                              &fsc[(buf ^ 1) * pg + warp]);
     if (nchunks > 1) __syncthreads();
   }
   if (any && !ok) {

@@ -1,7 +1,8 @@
-"""GPU parity of the large-M bf16 tensor-core path (w4a16_gemm_bf16) through the C ABI against
-the exact float64 product of the oracle: relative L2 <= 1e-2 (bf16 weights and output). Small
-cases cover one tile, ragged M and N and several K blocks; the full prefill workload
-(M=4096, K=7168, N=18432) is checked on sampled rows and columns."""
+"""GPU parity of w4a16_gemm_bf16 through the C ABI against the exact float64 product of the oracle:
+relative L2 <= 1e-2 (bf16 activations and output). Large M runs the tensor-core contraction, up
+to 16 rows the weight-streaming kernels in their bf16 form. Small cases cover one tile, ragged M
+and N and several K blocks; the full prefill workload (M=4096, K=7168, N=18432) and the full
+M=16 decode shape are checked on sampled rows and columns."""
 import numpy as np
 import pytest
 import torch
@@ -68,3 +69,42 @@ def test_prefill_full_size_sampled(w4):
     ref = oracle.gemm_bf16(xbits.view(np.uint16), qo, so)
     got = _as_f64(y)[rows][:, cols]
     assert_close_rows(got, ref, BF16_TOL, "prefill full size")
+
+
+# ---- bf16 activations at small M (weight-streaming kernels, bf16 form)
+
+@pytest.mark.parametrize("M,N,K", [(1, 264, 128), (3, 1000, 1024), (8, 520, 2048), (9, 256, 192),
+                                   (16, 1032, 4096)])
+def test_bf16_small_m(w4, M, N, K):
+    bits = synth.bf16_activations(M, K, seed=M + 7)
+    W = synth.weights(K, N, seed=K + M, outliers=True)
+    qo, so = oracle.quantize_w4a16(W)
+    y = w4.w4a16_gemm_bf16(_bf16_dev(bits), dev(qo), dev(so))
+    ref = oracle.gemm_bf16(bits, qo, so)
+    assert_close_rows(_as_f64(y), ref, BF16_TOL, f"bf16 small M={M} N={N} K={K}")
+    assert w4.w4a16_device_error() == 0
+
+
+def test_bf16_small_m_full_size_sampled(w4):
+    M, K, N = 16, synth.PREFILL["K"], synth.PREFILL["N"]
+    Wd = synth.cuda_weights(K, N, seed=3100)
+    qw, sc = w4.w4a16_quantize(Wd)
+    xb = synth.cuda_bf16_activations(M, K, seed=31)
+    y = w4.w4a16_gemm_bf16(xb, qw, sc)
+    torch.cuda.synchronize()
+    assert w4.w4a16_device_error() == 0
+    rng = np.random.default_rng(1)
+    cols = np.sort(np.concatenate([rng.choice(N, 126, replace=False), [0, N - 1]]))
+    Wc = host(Wd.index_select(1, torch.from_numpy(cols).cuda()))
+    qo, so = oracle.quantize_w4a16(Wc)
+    ref = oracle.gemm_bf16(xb.view(torch.int16).cpu().numpy().view(np.uint16), qo, so)
+    assert_close_rows(_as_f64(y)[:, cols], ref, BF16_TOL, "bf16 small M full size")
+
+
+def test_bf16_small_m_deterministic(w4):
+    M, N, K = 12, 768, 2048
+    bits = synth.bf16_activations(M, K, seed=5)
+    qo, so = oracle.quantize_w4a16(synth.weights(K, N, seed=5))
+    xd, qd, sd = _bf16_dev(bits), dev(qo), dev(so)
+    np.testing.assert_array_equal(_as_f64(w4.w4a16_gemm_bf16(xd, qd, sd)),
+                                  _as_f64(w4.w4a16_gemm_bf16(xd, qd, sd)))
