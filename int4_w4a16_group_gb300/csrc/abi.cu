@@ -13,6 +13,10 @@
 #include "../../include/w4a16.h"
 #include "internal.h"
 
+#ifndef W4A16_B16_STREAM_MAX_M
+#define W4A16_B16_STREAM_MAX_M 32
+#endif
+
 namespace w4a16 {
 
 namespace {
@@ -196,10 +200,17 @@ w4a16_status w4a16_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* 
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return cuda_status(e);
   if (di.cc_major != 10 || di.cc_minor != 3) return W4A16_ERR_UNSUPPORTED;
-  // Up to 16 rows the op is weight streaming: the small-M kernels (bf16 form) read each packed
-  // weight once; larger M is the tensor-core contraction.
-  e = M <= kGemvMaxM ? launch_gemv_b16(x, qw, sc, y, M, N, K, (cudaStream_t)stream)
-                     : launch_gemm_bf16(x, qw, sc, y, M, N, K, (cudaStream_t)stream);
+  // Up to W4A16_B16_STREAM_MAX_M rows the op is weight streaming (the small-M kernels in bf16
+  // form, 16-row slices); larger M is the tensor-core contraction.
+  if (M <= W4A16_B16_STREAM_MAX_M) {
+    for (int m0 = 0; m0 < M && e == cudaSuccess; m0 += kGemvMaxM) {
+      const int mc = M - m0 < kGemvMaxM ? M - m0 : kGemvMaxM;
+      e = launch_gemv_b16(x + (size_t)m0 * K, qw, sc, y + (size_t)m0 * N, mc, N, K,
+                          (cudaStream_t)stream);
+    }
+  } else {
+    e = launch_gemm_bf16(x, qw, sc, y, M, N, K, (cudaStream_t)stream);
+  }
   if (e == cudaErrorNotSupported) return W4A16_ERR_UNSUPPORTED;
   return cuda_status(e);
 }

@@ -29,7 +29,7 @@ namespace {
 
 using namespace mma;
 
-constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int BM = 128, BK = 64;
 // Two rings: the TMA ring of x tiles, codes and scales (kStagesA), and the ring of dequantized
 // bf16 B tiles (kStagesB), so TMA can run further ahead than the dequant warps need B tiles.
 #ifndef W4A16_PREFILL_STAGES_A
@@ -49,33 +49,37 @@ constexpr int kDeqWarp0 = 6;
 #endif
 constexpr int kDeqSplit = W4A16_PREFILL_DEQ_SPLIT;  // threads per weight column (groups per k-block split)
 static_assert(kDeqSplit == 1 || kDeqSplit == 2, "a 64-deep k-block holds two groups");
-constexpr int kDeqWarps = kDeqSplit * BN / 32;
-constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;
-constexpr int kAccCols = BN;
-constexpr int kTmemCols = 2 * kAccCols;
-
-constexpr int kABytes = BM * BK * 2;
-constexpr int kBBytes = BN * BK * 2;
-constexpr int kQBytes = (BK / 8) * BN * 4;
-constexpr int kSBytes = (BK / 32) * BN * 4;
-constexpr int kAOff = 0;
-constexpr int kQOff = kAOff + kStagesA * kABytes;
-constexpr int kSOff = kQOff + kStagesA * kQBytes;
-constexpr int kBOff = kSOff + kStagesA * kSBytes;  // 1024-aligned: SW128 tiles
-constexpr int kBarOff = kBOff + kStagesB * kBBytes;
-static_assert(kBOff % 1024 == 0, "B tiles need 1024-byte alignment");
-// barriers: full[SA] | empty[SA] | bready[SB] | bempty[SB] | accfull[2] | accempty[2] | drain
-constexpr int kFull = 0, kEmpty = kStagesA, kBReady = 2 * kStagesA,
-              kBEmpty = 2 * kStagesA + kStagesB, kAccFull = 2 * kStagesA + 2 * kStagesB,
-              kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2;
-constexpr int kNumBars = kDrain + 1;
-constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
-constexpr int kSmemBytes = kMiscOff + 16;
-constexpr int kSmemAlloc = kSmemBytes + 1024;
-constexpr uint32_t kStageTx = kABytes + kQBytes + kSBytes;
-
-// Instruction descriptor: bf16 x bf16 -> f32, M = 128, N = 256, both operands K-major.
-constexpr uint32_t kIdesc = tc::idesc_f16(true, BM, BN);
+// Everything that depends on the tile width BN (weight columns per tile: 256, or 128 when 256-wide
+// tiles would leave SMs idle).
+template <int BN_>
+struct PF {
+  static constexpr int BN = BN_;
+  static constexpr int kDeqWarps = kDeqSplit * BN / 32;
+  static constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;
+  static constexpr int kAccCols = BN;
+  static constexpr int kTmemCols = 2 * kAccCols;
+  static constexpr int kABytes = BM * BK * 2;
+  static constexpr int kBBytes = BN * BK * 2;
+  static constexpr int kQBytes = (BK / 8) * BN * 4;
+  static constexpr int kSBytes = (BK / 32) * BN * 4;
+  static constexpr int kAOff = 0;
+  static constexpr int kQOff = kAOff + kStagesA * kABytes;
+  static constexpr int kSOff = kQOff + kStagesA * kQBytes;
+  static constexpr int kBOff = ((kSOff + kStagesA * kSBytes + 1023) / 1024) * 1024;  // SW128 tiles
+  static constexpr int kBarOff = kBOff + kStagesB * kBBytes;
+  // barriers: full[SA] | empty[SA] | bready[SB] | bempty[SB] | accfull[2] | accempty[2] | drain
+  static constexpr int kFull = 0, kEmpty = kStagesA, kBReady = 2 * kStagesA,
+                       kBEmpty = 2 * kStagesA + kStagesB, kAccFull = 2 * kStagesA + 2 * kStagesB,
+                       kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2;
+  static constexpr int kNumBars = kDrain + 1;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static constexpr int kSmemAlloc = kSmemBytes + 1024;
+  static constexpr uint32_t kStageTx = kABytes + kQBytes + kSBytes;
+  // Instruction descriptor: bf16 x bf16 -> f32, M = 128, N = BN, both operands K-major.
+  static constexpr uint32_t kIdesc = tc::idesc_f16(true, BM, BN);
+  static_assert(kSmemAlloc <= 227 * 1024, "shared memory per CTA");
+};
 
 __device__ __forceinline__ uint32_t bf16x2_fma(uint32_t a, uint32_t b, uint32_t c) {
   uint32_t r;
@@ -112,39 +116,41 @@ __device__ __forceinline__ uint4 dequant_word_bf16(uint32_t w, uint32_t s2) {
   return o;
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+template <int BN>
+__global__ void __launch_bounds__(PF<BN>::kThreads, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap tmx, const __grid_constant__ CUtensorMap tmq,
                    const __grid_constant__ CUtensorMap tms, uint16_t* __restrict__ y, int M,
                    int N, int K, unsigned int* err) {
+  using C = PF<BN>;
   extern __shared__ __align__(1024) char smem_raw[];
   char* sm = align1024(smem_raw);
   const uint32_t sb = smem_u32(sm);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  auto bar = [&](int i) { return sb + kBarOff + 8u * (uint32_t)i; };
-  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + kMiscOff);
+  auto bar = [&](int i) { return sb + C::kBarOff + 8u * (uint32_t)i; };
+  volatile uint32_t* misc = reinterpret_cast<volatile uint32_t*>(sm + C::kMiscOff);
   const int mblocks = (M + BM - 1) / BM, nblocks = (N + BN - 1) / BN;
   const int tiles = mblocks * nblocks;
   const int kblocks = K / BK;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStagesA; ++s) {
-      mbar_init(bar(kFull + s), 1);
-      mbar_init(bar(kEmpty + s), 1);
+      mbar_init(bar(C::kFull + s), 1);
+      mbar_init(bar(C::kEmpty + s), 1);
     }
     for (int s = 0; s < kStagesB; ++s) {
-      mbar_init(bar(kBReady + s), kDeqWarps);
-      mbar_init(bar(kBEmpty + s), 1);
+      mbar_init(bar(C::kBReady + s), C::kDeqWarps);
+      mbar_init(bar(C::kBEmpty + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(kAccFull + b), 1);
-      mbar_init(bar(kAccEmpty + b), kEpiWarps);
+      mbar_init(bar(C::kAccFull + b), 1);
+      mbar_init(bar(C::kAccEmpty + b), kEpiWarps);
     }
-    mbar_init(bar(kDrain), 1);
+    mbar_init(bar(C::kDrain), 1);
     misc[1] = 0;
     mbar_fence_init();
   }
   if (warp == kMmaWarp) {
-    tc::tmem_alloc(sb + kMiscOff, kTmemCols);
+    tc::tmem_alloc(sb + C::kMiscOff, C::kTmemCols);
   }
   tc::fence_before();
   __syncthreads();
@@ -164,19 +170,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mb = tile % mblocks, nb = tile / mblocks;
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStagesA, use = it / kStagesA;
-          if (!mbar_wait(bar(kEmpty + s), (use & 1) ^ 1, kWaitLimitNs) || aborted()) {
+          if (!mbar_wait(bar(C::kEmpty + s), (use & 1) ^ 1, kWaitLimitNs) || aborted()) {
             fail();
             break;
           }
-          mbar_expect_tx(bar(kFull + s), kStageTx);
-          tma_load_3d(sb + kAOff + s * kABytes, &tmx, kb * BK, mb * BM, 0, bar(kFull + s));
-          tma_load_3d(sb + kQOff + s * kQBytes, &tmq, nb * BN, kb * (BK / 8), 0, bar(kFull + s));
-          tma_load_3d(sb + kSOff + s * kSBytes, &tms, nb * BN, kb * (BK / 32), 0, bar(kFull + s));
+          mbar_expect_tx(bar(C::kFull + s), C::kStageTx);
+          tma_load_3d(sb + C::kAOff + s * C::kABytes, &tmx, kb * BK, mb * BM, 0, bar(C::kFull + s));
+          tma_load_3d(sb + C::kQOff + s * C::kQBytes, &tmq, nb * BN, kb * (BK / 8), 0, bar(C::kFull + s));
+          tma_load_3d(sb + C::kSOff + s * C::kSBytes, &tms, nb * BN, kb * (BK / 32), 0, bar(C::kFull + s));
         }
       }
       // Let the last copies land before the CTA can exit (they target this CTA's memory).
       for (int j = (it > kStagesA ? it - kStagesA : 0); j < it; ++j)
-        (void)mbar_wait(bar(kFull + j % kStagesA), (j / kStagesA) & 1, kWaitLimitNs / 16);
+        (void)mbar_wait(bar(C::kFull + j % kStagesA), (j / kStagesA) & 1, kWaitLimitNs / 16);
     }
   } else if (warp >= kDeqWarp0) {
     // Thread = weight column n of the tile and, with two threads per column, group h of the
@@ -190,13 +196,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kb = 0; kb < kblocks; ++kb, ++it) {
         const int s = it % kStagesA, use = it / kStagesA;
         const int sbt = it % kStagesB, useb = it / kStagesB;
-        if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) ||
-            !mbar_wait(bar(kBEmpty + sbt), (useb & 1) ^ 1, kWaitLimitNs) || aborted()) {
+        if (!mbar_wait(bar(C::kFull + s), use & 1, kWaitLimitNs) ||
+            !mbar_wait(bar(C::kBEmpty + sbt), (useb & 1) ^ 1, kWaitLimitNs) || aborted()) {
           fail();
           break;
         }
-        const uint32_t q = sb + kQOff + s * kQBytes + (h * kWords * BN + n) * 4;
-        const uint32_t sc = sb + kSOff + s * kSBytes + n * 4;
+        const uint32_t q = sb + C::kQOff + s * C::kQBytes + (h * kWords * BN + n) * 4;
+        const uint32_t sc = sb + C::kSOff + s * C::kSBytes + n * 4;
         // bf16 scale pair of each group this thread covers (group g of the k-block = words
         // 4g .. 4g + 3).
         uint32_t s2[2];
@@ -206,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const __nv_bfloat162 hv = __floats2bfloat162_rn(sv, sv);
           s2[gq] = *reinterpret_cast<const uint32_t*>(&hv);
         }
-        const uint32_t bbase = sb + kBOff + sbt * kBBytes + brow;
+        const uint32_t bbase = sb + C::kBOff + sbt * C::kBBytes + brow;
 #pragma unroll
         for (int ii = 0; ii < kWords; ++ii) {
           const int i = h * kWords + ii;  // word (8 consecutive k) within the k-block
@@ -220,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc::fence_proxy_async();  // make the generic-proxy stores visible to the tensor cores
         __syncwarp();
-        if (lane == 0) tc::mbar_arrive(bar(kBReady + sbt));
+        if (lane == 0) tc::mbar_arrive(bar(C::kBReady + sbt));
       }
     }
   } else if (warp == kMmaWarp) {
@@ -229,49 +235,49 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       for (int tile = blockIdx.x; tile < tiles && ok && !aborted(); tile += gridDim.x, ++tcount) {
         const int b = tcount & 1, ause = tcount >> 1;
-        if (!mbar_wait(bar(kAccEmpty + b), (ause & 1) ^ 1, kWaitLimitNs)) {
+        if (!mbar_wait(bar(C::kAccEmpty + b), (ause & 1) ^ 1, kWaitLimitNs)) {
           fail();
           break;
         }
         tc::fence_after();
-        const uint32_t d_tmem = tmem + (uint32_t)(b * kAccCols);
+        const uint32_t d_tmem = tmem + (uint32_t)(b * C::kAccCols);
         for (int kb = 0; kb < kblocks; ++kb, ++it) {
           const int s = it % kStagesA, use = it / kStagesA;
           const int sbt = it % kStagesB, useb = it / kStagesB;
-          if (!mbar_wait(bar(kFull + s), use & 1, kWaitLimitNs) ||
-              !mbar_wait(bar(kBReady + sbt), useb & 1, kWaitLimitNs) || aborted()) {
+          if (!mbar_wait(bar(C::kFull + s), use & 1, kWaitLimitNs) ||
+              !mbar_wait(bar(C::kBReady + sbt), useb & 1, kWaitLimitNs) || aborted()) {
             fail();
             ok = false;
             break;
           }
           tc::fence_after();
-          const uint32_t a0 = sb + kAOff + s * kABytes, b0 = sb + kBOff + sbt * kBBytes;
+          const uint32_t a0 = sb + C::kAOff + s * C::kABytes, b0 = sb + C::kBOff + sbt * C::kBBytes;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk)
             tc::mma_ss(d_tmem, tc::sw128_desc(a0 + kk * 32), tc::sw128_desc(b0 + kk * 32),
-                       kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
-          tc::commit(bar(kEmpty + s));     // frees the x/codes stage once these MMAs read it
-          tc::commit(bar(kBEmpty + sbt));  // and the B tile
+                       C::kIdesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc::commit(bar(C::kEmpty + s));     // frees the x/codes stage once these MMAs read it
+          tc::commit(bar(C::kBEmpty + sbt));  // and the B tile
         }
         if (!ok) break;
-        tc::commit(bar(kAccFull + b));  // accumulator complete
+        tc::commit(bar(C::kAccFull + b));  // accumulator complete
       }
       // All MMAs issued by this thread have finished before TMEM is released.
-      tc::commit(bar(kDrain));
-      (void)mbar_wait(bar(kDrain), 0, kWaitLimitNs);
+      tc::commit(bar(C::kDrain));
+      (void)mbar_wait(bar(C::kDrain), 0, kWaitLimitNs);
     }
   } else {  // epilogue warps 0..3: TMEM lanes 32*warp .. 32*warp + 31 = tile rows
     int tcount = 0;
     for (int tile = blockIdx.x; tile < tiles && !aborted(); tile += gridDim.x, ++tcount) {
       const int mb = tile % mblocks, nb = tile / mblocks;
       const int b = tcount & 1, ause = tcount >> 1;
-      if (!mbar_wait(bar(kAccFull + b), ause & 1, kWaitLimitNs)) {
+      if (!mbar_wait(bar(C::kAccFull + b), ause & 1, kWaitLimitNs)) {
         fail();
         break;
       }
       tc::fence_after();
       const int row = mb * BM + warp * 32 + lane;
-      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * kAccCols);
+      const uint32_t tbase = tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(b * C::kAccCols);
 #pragma unroll 1
       for (int cc = 0; cc < BN / 32; ++cc) {
         uint32_t r[32];
@@ -296,34 +302,32 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) tc::mbar_arrive(bar(kAccEmpty + b));
+      if (lane == 0) tc::mbar_arrive(bar(C::kAccEmpty + b));
     }
   }
 
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, kTmemCols);
+  if (warp == kMmaWarp) tc::tmem_dealloc(tmem, C::kTmemCols);
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
-                             int M, int N, int K, cudaStream_t s) {
-  DeviceInfo di;
-  cudaError_t e = device_info(&di);
-  if (e != cudaSuccess) return e;
+template <int BN>
+cudaError_t launch_prefill(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
+                           int M, int N, int K, const DeviceInfo& di, cudaStream_t s) {
+  using C = PF<BN>;
   static int attr_devices = 0;
   const int bit = 1 << (di.device & 31);
   if (!(attr_devices & bit)) {
-    e = cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc);
+    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         C::kSmemAlloc);
     if (e != cudaSuccess) return e;
     attr_devices |= bit;
   }
   CUtensorMap tmx, tmq, tms;
-  e = make_tmap_ex(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, CU_TENSOR_MAP_SWIZZLE_128B, x,
-                   (uint64_t)K, (uint64_t)M, 1, BK, BM);
+  cudaError_t e = make_tmap_ex(&tmx, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                               CU_TENSOR_MAP_SWIZZLE_128B, x, (uint64_t)K, (uint64_t)M, 1, BK, BM);
   if (e != cudaSuccess) return e;
   e = make_tmap_ex(&tmq, CU_TENSOR_MAP_DATA_TYPE_INT32, 4, CU_TENSOR_MAP_SWIZZLE_NONE, qw,
                    (uint64_t)N, (uint64_t)(K / 8), 1, BN, BK / 8);
@@ -333,9 +337,23 @@ cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* 
   if (e != cudaSuccess) return e;
   const int tiles = ((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const int grid = tiles < di.sm_count ? tiles : di.sm_count;
-  prefill_kernel<<<grid, kThreads, kSmemAlloc, s>>>(tmx, tmq, tms, y, M, N, K,
-                                                     device_error_word());
+  prefill_kernel<BN><<<grid, C::kThreads, C::kSmemAlloc, s>>>(tmx, tmq, tms, y, M, N, K,
+                                                                device_error_word());
   return cudaGetLastError();
+}
+
+}  // namespace
+
+// 128 x 256 tiles by default; 128 x 128 tiles when even twice as many tiles fit in one wave over
+// the SMs (then the wide tiles would leave more than half of them idle).
+cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
+                             int M, int N, int K, cudaStream_t s) {
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  const long long wide_tiles = (long long)((M + BM - 1) / BM) * ((N + 255) / 256);
+  return 2 * wide_tiles <= di.sm_count ? launch_prefill<128>(x, qw, sc, y, M, N, K, di, s)
+                                       : launch_prefill<256>(x, qw, sc, y, M, N, K, di, s);
 }
 
 }  // namespace w4a16
