@@ -379,7 +379,25 @@ def other_workloads(args, w4, peaks, stream):
                                 "GB/s": mb / (us * 1e-6) / 1e9,
                                 "frac_of_hbm": mb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
                                 "launches_per_call": 4}
-    del gq, gs, dq, ds, ws
+    del ws
+
+    # the same block with a shared expert (I = 2048) that all 64 rows go through
+    a, b = synth.cuda_moe_expert_weights(E, K, I, seed=1)
+    sgq, sgs = w4.w4a16_quantize(a)
+    sdq, sds = w4.w4a16_quantize(b)
+    del a, b
+    ws = torch.empty(w4.w4a16_moe_block_workspace_size(T, topk, E, K, I, I), dtype=torch.uint8,
+                     device="cuda")
+    fns = [lambda: w4.w4a16_moe_block(x, idd, wts, gq, gs, dq, ds, sgq, sgs, sdq, sds, out, ws,
+                                      stream=stream) for _ in range(reps + 3)]
+    t = _time_launches(stream, fns)[3:]
+    us = 1e3 * statistics.mean(t)
+    mbs = mb + BYTES_PER_WEIGHT * (K * 2 * I + I * K)  # every weight byte counted once
+    res["moe_block_T64_E384_top8_shared"] = {
+        "us": us, "active_experts": active, "algorithmic_bytes": mbs,
+        "GB/s": mbs / (us * 1e-6) / 1e9, "frac_of_hbm": mbs / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+        "launches_per_call": 4 + 2 * ((T + 15) // 16)}
+    del gq, gs, dq, ds, ws, sgq, sgs, sdq, sds
 
     # large-M bf16 contraction (tensor cores)
     c = synth.PREFILL

@@ -132,6 +132,28 @@ w4a16_status w4a16_moe_gemm(const float* x, const int32_t* topk_ids, const float
                             float* out, int K, int I, int group,
                             void* workspace, size_t ws_bytes, w4a16_stream_t stream);
 
+/* MoE block with a shared expert (page "The Weight of Precision ...", section "The Engine
+ * Dispatch: Model::linear": the MoE experts, the shared expert and the dense MLP layers run
+ * through the INT4 path):
+ *   out[t, :] = down_s( silu(g_s) * u_s ) + sum_{j < topk} topk_w[t, j] * down_e(...),
+ *   (g_s | u_s) = x[t] @ W_gu_shared,
+ * i.e. w4a16_moe_gemm plus one expert that every token goes through with weight 1.
+ *   qs_gu [K/8, 2 Is] int32, ss_gu [K/32, 2 Is] float32   (gate | up of the shared expert)
+ *   qs_dn [Is/8, K] int32,   ss_dn [Is/32, K] float32
+ * Other arguments as w4a16_moe_gemm; Is a multiple of 32; the shared expert's weights 16-byte
+ * aligned. `workspace` holds at least w4a16_moe_block_workspace_size(T, topk, E, K, I, Is) bytes.
+ * The shared expert runs as dense small-M GEMMs in 16-row slices; its output seeds each row of the
+ * combine, which then adds the routed rows in slot order. Deterministic. */
+size_t w4a16_moe_block_workspace_size(int T, int topk, int E, int K, int I, int Is);
+w4a16_status w4a16_moe_block(const float* x, const int32_t* topk_ids, const float* topk_w,
+                             int T, int topk, int E,
+                             const int32_t* qw_gu, const float* sc_gu,
+                             const int32_t* qw_dn, const float* sc_dn,
+                             const int32_t* qs_gu, const float* ss_gu,
+                             const int32_t* qs_dn, const float* ss_dn, int Is,
+                             float* out, int K, int I, int group,
+                             void* workspace, size_t ws_bytes, w4a16_stream_t stream);
+
 /* The same MoE block for callers that cannot allocate device memory, such as a plugin or
  * foreign-function interface that only passes input and output buffers, or a process whose
  * device memory another runtime has already reserved. The pages have no counterpart: this is

@@ -40,6 +40,9 @@ _SIGS = {
     "w4a16_moe_workspace_size": (_sz, [_i, _i, _i, _i, _i]),
     "w4a16_moe_gemm": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p]),
     "w4a16_moe_gemm_noalloc": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
+    "w4a16_moe_block_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "w4a16_moe_block": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i,
+                             _i, _p, _sz, _p]),
     "w4a16_topk_softmax": (_i, [_p, _p, _i, _i, _p]),
     "w4a16_load_qw_sc": (_i, [_s, _s, _i, _i, _i, _p, _p]),
     "w4a16_registry_create": (_p, []),
@@ -206,6 +209,40 @@ def w4a16_moe_gemm(x, topk_ids, topk_w, qw_gu, sc_gu, qw_dn, sc_dn, out=None, wo
         _dev(out, torch.float32, "out", (T, K)), K, I, group,
         _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)),
         "w4a16_moe_gemm")
+    return out
+
+
+def w4a16_moe_block_workspace_size(T: int, topk: int, E: int, K: int, I: int, Is: int) -> int:
+    return int(_lib.w4a16_moe_block_workspace_size(T, topk, E, K, I, Is))
+
+
+def w4a16_moe_block(x, topk_ids, topk_w, qw_gu, sc_gu, qw_dn, sc_dn, qs_gu, ss_gu, qs_dn, ss_dn,
+                    out=None, workspace=None, group: int = GROUP, stream=None):
+    """MoE block with a shared expert; see w4a16.h. Returns out[T, K]."""
+    T, K = x.shape
+    topk = topk_ids.shape[1]
+    E = qw_gu.shape[0]
+    I = qw_gu.shape[2] // 2
+    Is = qs_gu.shape[1] // 2
+    if out is None:
+        out = torch.empty((T, K), dtype=torch.float32, device=x.device)
+    need = w4a16_moe_block_workspace_size(T, topk, E, K, I, Is)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    _check(_lib.w4a16_moe_block(
+        _dev(x, torch.float32, "x"), _dev(topk_ids, torch.int32, "topk_ids", (T, topk)),
+        _dev(topk_w, torch.float32, "topk_w", (T, topk)), T, topk, E,
+        _dev(qw_gu, torch.int32, "qw_gu", (E, K // 8, 2 * I)),
+        _dev(sc_gu, torch.float32, "sc_gu", (E, K // GROUP, 2 * I)),
+        _dev(qw_dn, torch.int32, "qw_dn", (E, I // 8, K)),
+        _dev(sc_dn, torch.float32, "sc_dn", (E, I // GROUP, K)),
+        _dev(qs_gu, torch.int32, "qs_gu", (K // 8, 2 * Is)),
+        _dev(ss_gu, torch.float32, "ss_gu", (K // GROUP, 2 * Is)),
+        _dev(qs_dn, torch.int32, "qs_dn", (Is // 8, K)),
+        _dev(ss_dn, torch.float32, "ss_dn", (Is // GROUP, K)), Is,
+        _dev(out, torch.float32, "out", (T, K)), K, I, group,
+        _dev(workspace, torch.uint8, "workspace"), workspace.numel(), _stream(stream)),
+        "w4a16_moe_block")
     return out
 
 

@@ -241,6 +241,38 @@ w4a16_status w4a16_moe_gemm(const float* x, const int32_t* topk_ids, const float
                                 K, I, workspace, ws_bytes, (cudaStream_t)stream));
 }
 
+size_t w4a16_moe_block_workspace_size(int T, int topk, int E, int K, int I, int Is) {
+  if (T < 0 || topk <= 0 || E <= 0 || K <= 0 || I <= 0 || Is <= 0) return 0;
+  return moe_block_workspace_size(T, topk, E, K, I, Is);
+}
+
+w4a16_status w4a16_moe_block(const float* x, const int32_t* topk_ids, const float* topk_w, int T,
+                             int topk, int E, const int32_t* qw_gu, const float* sc_gu,
+                             const int32_t* qw_dn, const float* sc_dn, const int32_t* qs_gu,
+                             const float* ss_gu, const int32_t* qs_dn, const float* ss_dn, int Is,
+                             float* out, int K, int I, int group, void* workspace,
+                             size_t ws_bytes, w4a16_stream_t stream) {
+  if (group != W4A16_GROUP) return W4A16_ERR_UNSUPPORTED;
+  if (T < 0 || topk <= 0 || topk > 64 || E <= 0 || E > 4096) return W4A16_ERR_ARG;
+  if (K <= 0 || K % W4A16_GROUP != 0 || I <= 0 || I % W4A16_GROUP != 0 || Is <= 0 ||
+      Is % W4A16_GROUP != 0)
+    return W4A16_ERR_ARG;
+  if (T == 0) return W4A16_OK;
+  if (!x || !topk_ids || !topk_w || !qw_gu || !sc_gu || !qw_dn || !sc_dn || !qs_gu || !ss_gu ||
+      !qs_dn || !ss_dn || !out)
+    return W4A16_ERR_ARG;
+  if (!aligned16(x) || !aligned16(qw_gu) || !aligned16(sc_gu) || !aligned16(qw_dn) ||
+      !aligned16(sc_dn) || !aligned16(qs_gu) || !aligned16(ss_gu) || !aligned16(qs_dn) ||
+      !aligned16(ss_dn) || !aligned16(out) || !aligned16(topk_ids) || !aligned16(topk_w))
+    return W4A16_ERR_ALIGN;
+  const size_t need = moe_block_workspace_size(T, topk, E, K, I, Is);
+  if (!workspace || ws_bytes < need) return W4A16_ERR_WORKSPACE;
+  if (!aligned16(workspace)) return W4A16_ERR_ALIGN;
+  return cuda_status(launch_moe_block(x, topk_ids, topk_w, T, topk, E, qw_gu, sc_gu, qw_dn, sc_dn,
+                                      qs_gu, ss_gu, qs_dn, ss_dn, Is, out, K, I, workspace,
+                                      ws_bytes, (cudaStream_t)stream));
+}
+
 w4a16_status w4a16_topk_softmax(const float* logits, float* weights, int T, int topk,
                                 w4a16_stream_t stream) {
   if (T < 0 || topk <= 0 || topk > 32) return W4A16_ERR_ARG;

@@ -55,6 +55,13 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
                        int E, const int32_t* qw_gu, const float* sc_gu, const int32_t* qw_dn,
                        const float* sc_dn, float* out, int K, int I, void* ws, size_t ws_bytes,
                        cudaStream_t s);
+size_t moe_block_workspace_size(int T, int topk, int E, int K, int I, int Is);
+cudaError_t launch_moe_block(const float* x, const int32_t* ids, const float* w, int T, int topk,
+                             int E, const int32_t* qw_gu, const float* sc_gu,
+                             const int32_t* qw_dn, const float* sc_dn, const int32_t* qs_gu,
+                             const float* ss_gu, const int32_t* qs_dn, const float* ss_dn, int Is,
+                             float* out, int K, int I, void* ws, size_t ws_bytes,
+                             cudaStream_t s);
 cudaError_t launch_topk_softmax(const float* logits, float* weights, int T, int topk,
                                 cudaStream_t s);
 

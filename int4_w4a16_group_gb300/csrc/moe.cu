@@ -11,7 +11,8 @@
 //                 rows (up to 8 per pass) with the tensor-core core of mma_core.cuh and writes
 //                 silu(g)*u rows of h[pairs, I] in expert-sorted order;
 //   3. down     : same over (active expert, 512-column tile) of the down weights, h -> y_pair;
-//   4. combine  : out[t] = sum_j topk_w[t, j] * y_pair[pos(t, j)] in slot order.
+//   4. combine  : out[t] = sum_j topk_w[t, j] * y_pair[pos(t, j)] in slot order (the MoE block
+//                 entry first runs a shared expert and starts each row from its output).
 // No atomics on data, so the result is deterministic. Every weight byte of an active expert is
 // read once per call (plus one more pass per further 8 rows for experts with more than 8).
 #include <stdint.h>
@@ -180,16 +181,19 @@ __global__ void __launch_bounds__(kWN * 32, 2)
 
 // ---------------------------------------------------------------------------------- combine
 
+// With `shared` (the shared expert's output [T, K]) each row starts from it, then adds the routed
+// rows in slot order.
 __global__ void moe_combine_kernel(const float* __restrict__ ypair, const int* __restrict__ pos,
                                    const float* __restrict__ w, int T, int topk, int K,
-                                   float* __restrict__ out) {
+                                   const float* __restrict__ shared, float* __restrict__ out) {
   const int K4 = K >> 2;
   const long long total = (long long)T * K4;
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
     const int t = (int)(idx / K4);
     const int c4 = (int)(idx - (long long)t * K4);
-    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 s = shared ? reinterpret_cast<const float4*>(shared + (size_t)t * K)[c4]
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < topk; ++j) {
       const int p = pos[t * topk + j];
       if (p < 0) continue;
@@ -258,10 +262,28 @@ size_t moe_workspace_size(int T, int topk, int E, int K, int I) {
   return moe_layout(T, topk, E, K, I).total;
 }
 
+size_t moe_block_workspace_size(int T, int topk, int E, int K, int I, int Is) {
+  return moe_layout(T, topk, E, K, I).total + align256((size_t)T * Is * sizeof(float)) +
+         align256((size_t)T * K * sizeof(float));
+}
+
 cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T, int topk, int E,
                        const int32_t* qw_gu, const float* sc_gu, const int32_t* qw_dn,
                        const float* sc_dn, float* out, int K, int I, void* ws, size_t ws_bytes,
                        cudaStream_t s) {
+  return launch_moe_block(x, ids, w, T, topk, E, qw_gu, sc_gu, qw_dn, sc_dn, nullptr, nullptr,
+                          nullptr, nullptr, 0, out, K, I, ws, ws_bytes, s);
+}
+
+// The routed experts as in launch_moe, plus (when qs_gu is given) a shared expert that every
+// token goes through with weight 1: its gate/up + SwiGLU and down projections run as dense
+// small-M GEMMs in 16-row slices into the workspace, and the combine starts each row from it.
+cudaError_t launch_moe_block(const float* x, const int32_t* ids, const float* w, int T, int topk,
+                             int E, const int32_t* qw_gu, const float* sc_gu,
+                             const int32_t* qw_dn, const float* sc_dn, const int32_t* qs_gu,
+                             const float* ss_gu, const int32_t* qs_dn, const float* ss_dn, int Is,
+                             float* out, int K, int I, void* ws, size_t ws_bytes,
+                             cudaStream_t s) {
   (void)ws_bytes;
   DeviceInfo di;
   cudaError_t e = device_info(&di);
@@ -308,11 +330,26 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
   dn.ldd = K;
   if ((e = launch_grouped<false>(dn, qw_dn, sc_dn, E, di, s)) != cudaSuccess) return e;
 
+  float* ys = nullptr;
+  if (qs_gu) {
+    float* hs = reinterpret_cast<float*>(base + L.total);
+    ys = reinterpret_cast<float*>(base + L.total + align256((size_t)T * Is * sizeof(float)));
+    for (int m0 = 0; m0 < T; m0 += kGemvMaxM) {
+      const int mc = T - m0 < kGemvMaxM ? T - m0 : kGemvMaxM;
+      if ((e = launch_gemv(x + (size_t)m0 * K, qs_gu, ss_gu, hs + (size_t)m0 * Is, mc, 2 * Is, K,
+                           true, s)) != cudaSuccess)
+        return e;
+      if ((e = launch_gemv(hs + (size_t)m0 * Is, qs_dn, ss_dn, ys + (size_t)m0 * K, mc, K, Is,
+                           false, s)) != cudaSuccess)
+        return e;
+    }
+  }
+
   const long long total4 = (long long)T * (K / 4);
   long long blocks = (total4 + 255) / 256;
   if (blocks > (long long)di.sm_count * 16) blocks = (long long)di.sm_count * 16;
   moe_combine_kernel<<<(int)(blocks < 1 ? 1 : blocks), 256, 0, s>>>(ypair, pos, w, T, topk, K,
-                                                                    out);
+                                                                    ys, out);
   return cudaGetLastError();
 }
 

@@ -15,6 +15,7 @@ from .w4a16_ref import (  # noqa: F401
     silu,
     swiglu_gemm,
     topk_softmax,
+    moe_block_forward,
     moe_forward,
     bf16_bits_to_f64,
     gemm_bf16,

@@ -186,6 +186,21 @@ def moe_forward(x, topk_ids, topk_w, gate_up, down, group: int = GROUP) -> np.nd
     return out
 
 
+def moe_block_forward(x, topk_ids, topk_w, gate_up, down, shared_gate_up, shared_down,
+                      group: int = GROUP) -> np.ndarray:
+    """MoE block with a shared expert, float64: the routed sum of moe_forward plus one expert
+    that every token goes through with weight 1,
+
+    out[t] = down_s(swiglu(gate_up_s(x[t]))) + sum_{slot} topk_w[t, slot] * down_e(...)
+
+    ``shared_gate_up`` and ``shared_down`` are (qw, sc) pairs.
+    [Weight of Precision] "The Engine Dispatch: Model::linear": the MoE experts, the shared expert
+    and the dense MLP layers run through the INT4 path."""
+    routed = moe_forward(x, topk_ids, topk_w, gate_up, down, group)
+    shared = gemm(swiglu_gemm(x, *shared_gate_up, group), *shared_down, group)
+    return routed + shared
+
+
 # ------------------------------------------------------------------------------------- bf16 prefill
 
 def bf16_bits_to_f64(bits: np.ndarray) -> np.ndarray:

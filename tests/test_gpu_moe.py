@@ -1,7 +1,8 @@
 """GPU parity of the routed-expert MoE block (w4a16_moe_gemm) and of the router softmax,
 through the C ABI, against the oracle. Small cases cover skewed routing (one expert receiving
 more rows than one pass holds), unused experts, ragged widths and top-1; the full-size
-tree-verify workload (T=64, E=384, top-8) is checked on sampled tokens."""
+tree-verify workload (T=64, E=384, top-8) is checked on sampled tokens, with and without a
+shared expert (w4a16_moe_block)."""
 import numpy as np
 import pytest
 import torch
@@ -126,3 +127,37 @@ def test_full_size_tree_verify_moe(w4):
     ref = oracle.moe_forward(x[toks], ids[toks], oracle.topk_softmax(logits[toks]),
                              gu_o.__getitem__, dn_o.__getitem__)
     assert_close_rows(out[toks], ref, FP32_TOL, "full-size moe")
+
+    # the same block with a shared expert of the routed experts' width
+    a, b = synth.cuda_moe_expert_weights(E, K, I, seed=seed + 1)
+    sgq, sgs = w4.w4a16_quantize(a)
+    sdq, sds = w4.w4a16_quantize(b)
+    sgu_o, sdn_o = oracle.quantize_w4a16(host(a)), oracle.quantize_w4a16(host(b))
+    del a, b
+    blk = host(w4.w4a16_moe_block(dev(x), dev(ids), wts, gq, gs, dq, ds, sgq, sgs, sdq, sds))
+    assert w4.w4a16_device_error() == 0
+    ref = oracle.moe_block_forward(x[toks], ids[toks], oracle.topk_softmax(logits[toks]),
+                                   gu_o.__getitem__, dn_o.__getitem__, sgu_o, sdn_o)
+    assert_close_rows(blk[toks], ref, FP32_TOL, "full-size moe block")
+
+
+@pytest.mark.parametrize("T,E,topk,K,I,Is", [
+    (5, 6, 3, 128, 64, 96),
+    (20, 8, 2, 256, 96, 64),         # 20 tokens: two 16-row slices of the shared expert
+    (7, 5, 1, 64, 64, 32),
+])
+def test_moe_block_with_shared_expert(w4, T, E, topk, K, I, Is):
+    seed = T + E + Is
+    ids, logits = synth.routing(T, E, topk, seed=seed)
+    x = synth.activations(T, K, seed=seed)
+    gu_o, dn_o, (gq, gs, dq, ds) = _experts(w4, E, K, I, seed)
+    a, b = synth.moe_expert_weights(99, K, Is, seed=seed)
+    sgu_o, sdn_o = oracle.quantize_w4a16(a), oracle.quantize_w4a16(b)
+    sgq, sgs = w4.w4a16_quantize(dev(a))
+    sdq, sds = w4.w4a16_quantize(dev(b))
+    wts = w4.w4a16_topk_softmax(dev(logits))
+    out = w4.w4a16_moe_block(dev(x), dev(ids), wts, gq, gs, dq, ds, sgq, sgs, sdq, sds)
+    ref = oracle.moe_block_forward(x, ids, oracle.topk_softmax(logits), gu_o.__getitem__,
+                                   dn_o.__getitem__, sgu_o, sdn_o)
+    assert_close_rows(host(out), ref, FP32_TOL, "moe block")
+    assert w4.w4a16_device_error() == 0

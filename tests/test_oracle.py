@@ -278,6 +278,54 @@ def test_moe_weights_scale_linearly():
     assert (z == 0).all()
 
 
+def _mlp_brute_force(x_row, qgu, qdn):
+    """One token through one expert's SwiGLU MLP with scalar exact sums."""
+    deq_gu = oracle.dequantize(*qgu)
+    deq_dn = oracle.dequantize(*qdn)
+    hh = [math.fsum(float(x_row[k]) * deq_gu[k, n] for k in range(len(x_row)))
+          for n in range(deq_gu.shape[1])]
+    I = len(hh) // 2
+    act = [hh[i] / (1.0 + math.exp(-hh[i])) * hh[I + i] for i in range(I)]
+    return np.array([math.fsum(act[i] * deq_dn[i, n] for i in range(I))
+                     for n in range(deq_dn.shape[1])])
+
+
+def _shared_expert(K=64, Is=64, seed=9):
+    wg, wd = synth.moe_expert_weights(100, K, Is, seed=seed)
+    return oracle.quantize_w4a16(wg), oracle.quantize_w4a16(wd)
+
+
+def test_moe_block_brute_force():
+    x, ids, logits, gu, dn = _tiny_moe(seed=2)
+    sgu, sdn = _shared_expert()
+    w = oracle.topk_softmax(logits)
+    got = oracle.moe_block_forward(x, ids, w, gu.__getitem__, dn.__getitem__, sgu, sdn)
+    T, topk = ids.shape
+    for t in range(T):
+        want = _mlp_brute_force(x[t], sgu, sdn)
+        for j in range(topk):
+            e = int(ids[t, j])
+            want = want + w[t, j] * _mlp_brute_force(x[t], gu[e], dn[e])
+        np.testing.assert_allclose(got[t], want, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_block_reduces_to_its_parts():
+    """Zero shared weights give the routed block; zero router weights give the shared MLP."""
+    x, ids, logits, gu, dn = _tiny_moe(seed=3)
+    sgu, sdn = _shared_expert(seed=4)
+    w = oracle.topk_softmax(logits)
+    zgu = oracle.quantize_w4a16(np.zeros((64, 128), dtype=np.float32))
+    zdn = oracle.quantize_w4a16(np.zeros((64, 64), dtype=np.float32))
+    routed = oracle.moe_forward(x, ids, w, gu.__getitem__, dn.__getitem__)
+    np.testing.assert_array_equal(
+        oracle.moe_block_forward(x, ids, w, gu.__getitem__, dn.__getitem__, zgu, zdn), routed)
+    only_shared = oracle.moe_block_forward(x, ids, np.zeros_like(w), gu.__getitem__,
+                                           dn.__getitem__, sgu, sdn)
+    for t in range(x.shape[0]):
+        np.testing.assert_allclose(only_shared[t], _mlp_brute_force(x[t], sgu, sdn), rtol=1e-12,
+                                   atol=1e-14)
+
+
 # ----------------------------------------------------------------------------- bf16
 
 def test_bf16_decode_matches_torch():
