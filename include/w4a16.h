@@ -214,6 +214,23 @@ w4a16_status w4a16_linear(const w4a16_registry* reg, const char* name, const flo
 w4a16_status w4a16_linear_swiglu(const w4a16_registry* reg, const char* name, const float* x,
                                  float* y, int M, w4a16_stream_t stream);
 
+/* Multi-tensor weight bundle (page "The Final Wire ...", section "The Multi-Step Integration
+ * Chain", steps 3 and 5: a generator writes bundles of quantized weights and scales; the engine
+ * maps weight names to them). The pages give no byte layout; this library's is, little-endian:
+ *   "W4A16BDL" (8 bytes), u32 version = 1, u32 count,
+ *   count x { u32 name_len, name (no terminator), i32 K, i32 N, u64 qw_offset, u64 sc_offset },
+ *   then the blobs qw [K/8, N] int32 and sc [K/32, N] float32 at their file offsets.
+ * Names are unique, K a multiple of 32, N of 4. w4a16_bundle_info reads the index only and
+ * reports the number of tensors and the device bytes w4a16_bundle_load needs. w4a16_bundle_load
+ * copies every tensor into `arena` (caller-owned device memory, 256-byte aligned, each blob at
+ * a 256-byte boundary), synchronously, and adds each name to `reg`, which then points into the
+ * arena. W4A16_ERR_IO for an unreadable or malformed file (nothing is copied for a malformed
+ * index), W4A16_ERR_WORKSPACE for a too small arena. The Python writer is
+ * int4_w4a16_group_gb300/bundle.py. */
+w4a16_status w4a16_bundle_info(const char* path, int* count, size_t* device_bytes);
+w4a16_status w4a16_bundle_load(w4a16_registry* reg, const char* path, void* arena,
+                               size_t arena_bytes);
+
 /* ------------------------------------------------------------------------------------------
  * Device error word. Kernels that wait on a barrier give up after a bounded number of polls
  * and record a status here instead of hanging. Synchronizes the device, returns the recorded

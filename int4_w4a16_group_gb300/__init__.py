@@ -6,7 +6,8 @@ package is a thin ctypes binding over it. The binding loads on first use of any 
 first use raises ImportError when the library has not been built.
 """
 _EXPORTS = (
-    "C", "GROUP", "LIB_PATH", "Registry", "W4A16Error", "w4a16_abi_version", "w4a16_dequantize",
+    "C", "GROUP", "LIB_PATH", "Registry", "W4A16Error", "bundle_info", "w4a16_abi_version",
+    "w4a16_dequantize",
     "w4a16_device_error", "w4a16_gemm", "w4a16_gemm_bf16", "w4a16_gemm_swiglu",
     "w4a16_load_qw_sc", "w4a16_moe_block", "w4a16_moe_block_workspace_size", "w4a16_moe_gemm",
     "w4a16_moe_gemm_noalloc", "w4a16_moe_workspace_size", "w4a16_quantize",

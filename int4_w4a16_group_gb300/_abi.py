@@ -41,6 +41,8 @@ _SIGS = {
     "w4a16_moe_gemm": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p, _sz, _p]),
     "w4a16_moe_gemm_noalloc": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _i, _i, _i, _p]),
     "w4a16_moe_block_workspace_size": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "w4a16_bundle_info": (_i, [_s, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)]),
+    "w4a16_bundle_load": (_i, [_p, _s, _p, _sz]),
     "w4a16_moe_block": (_i, [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _p, _i, _i,
                              _i, _p, _sz, _p]),
     "w4a16_topk_softmax": (_i, [_p, _p, _i, _i, _p]),
@@ -292,6 +294,14 @@ def w4a16_device_error() -> int:
     return code.value
 
 
+def bundle_info(path: str):
+    """(number of tensors, device bytes needed) of a weight bundle (w4a16_bundle_info)."""
+    count, nbytes = ctypes.c_int(0), ctypes.c_size_t(0)
+    _check(_lib.w4a16_bundle_info(str(path).encode(), ctypes.byref(count), ctypes.byref(nbytes)),
+           f"w4a16_bundle_info({path})")
+    return count.value, nbytes.value
+
+
 class Registry:
     """Name -> quantized weight map with linear() dispatch (w4a16_registry_* / w4a16_linear*).
 
@@ -320,6 +330,15 @@ class Registry:
                                        _dev(sc, torch.float32, "sc", (K8 * 8 // GROUP, N)), K8 * 8, N,
                                        group), f"w4a16_registry_add({name})")
         self._keep[name] = (qw, sc)
+
+    def load_bundle(self, path: str, device="cuda") -> torch.Tensor:
+        """Loads every tensor of a weight bundle (w4a16_bundle_load) into one device arena and
+        registers its names; returns the arena, which the registry also keeps alive."""
+        arena = torch.empty(max(bundle_info(path)[1], 256), dtype=torch.uint8, device=device)
+        _check(_lib.w4a16_bundle_load(self._h, str(path).encode(), arena.data_ptr(),
+                                      arena.numel()), f"w4a16_bundle_load({path})")
+        self._keep[("bundle", str(path))] = arena
+        return arena
 
     def find(self, name: str):
         K, N = ctypes.c_int(0), ctypes.c_int(0)
