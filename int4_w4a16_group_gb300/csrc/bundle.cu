@@ -130,7 +130,8 @@ w4a16_status w4a16_bundle_load(w4a16_registry* reg, const char* path, void* aren
     char* dsts[2] = {qd, sd};
     for (int k = 0; k < 2; ++k) {
       buf.resize(sizes[k]);
-      if (fseeko(file.f, (off_t)offs[k], SEEK_SET) != 0 || !read_exact(file.f, buf.data(), sizes[k]))
+      if (fseeko(file.f, (off_t)offs[k], SEEK_SET) != 0 ||
+          !read_exact(file.f, buf.data(), sizes[k]))
         return W4A16_ERR_IO;
       const cudaError_t ce = cudaMemcpy(dsts[k], buf.data(), sizes[k], cudaMemcpyHostToDevice);
       if (ce != cudaSuccess) return W4A16_ERR_CUDA;

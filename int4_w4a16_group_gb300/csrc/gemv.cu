@@ -1,4 +1,5 @@
-// Small-M (decode / draft-tree verify) weight-streaming GEMM: y = x @ dequant(W), float32.
+// Small-M (decode / draft-tree verify) weight-streaming GEMM: y = x @ dequant(W), float32
+// activations and output (also in a bf16 form: bf16 activations and output, M <= 16).
 //
 // Page "The Weight of Precision: Building Native INT4 Quantization for a Custom Speculative
 // Decoding Engine", section "The Kernel: w4a16_gemm" (FP32 activations, packed INT4 weights,

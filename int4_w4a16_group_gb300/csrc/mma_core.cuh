@@ -2,10 +2,10 @@
 //
 // Each warp owns a slice of 32*CH weight columns and walks the CTA's K range two groups
 // (2 x 32 k) per pipeline stage. Per stage it:
-//   * receives, by TMA (one elected lane issues 2*CH tile copies into a 4-stage ring with an
-//     mbarrier per stage), CH tiles of 32 columns x 8 packed rows of the codes (128-byte
-//     swizzle, so the lanes' 16-byte reads below are bank-conflict free) and CH tiles of
-//     32 columns x 2 rows of the scales;
+//   * receives, by TMA (one elected lane issues 2*CH tile copies into the warp's ring of R
+//     stages, 2 to 4 by geometry, with an mbarrier per stage), CH tiles of 32 columns x 8 packed
+//     rows of the codes (128-byte swizzle, so the lanes' 16-byte reads below are bank-conflict
+//     free) and CH tiles of 32 columns x 2 rows of the scales;
 //   * turns each lane's 4 words per tile into fp16 MMA A-fragments with two bit tricks:
 //     (w & 0x000F000F) | 0x64006400 is the fp16 pair (1024 + nibble_0, 1024 + nibble_4), and the
 //     same mask shifted by 4 gives 1024 + 16 * nibble; one fp16 FMA then yields nibble - 8;
@@ -15,6 +15,8 @@
 //   * applies the group scale times 2^e to the fresh fp32 group sums with one FMA each.
 // The unpacked codes are exact integers, products of codes and fp16 terms are exact in fp32,
 // so the only rounding beyond float32 accumulation is the ~2^-22 relative cut of x.
+// A bf16 mode (stream_groups<..., B16 = true>) serves bf16 activations: the codes unpack to
+// bf16 instead, and the activations are MMA operands as they are (no split, no exponent).
 //
 // MMA operand mapping (m16n8k16; g = lane / 4, t = lane % 4):
 //   A (16 x 16): rows = weight columns, k = input index. Lane (g, t) holds the packed word of

@@ -3,19 +3,21 @@
 // The pages' activations are float32 and their kernel has no large-M form; this path serves
 // batched prefill, where the op really is a dense contraction.
 //
-// Persistent CTAs (one per SM) walk 128 x 256 output tiles, M-blocks fastest (so the x tiles of
-// a weight block are reused from L2). Per 64-deep K block of a tile:
+// Persistent CTAs (one per SM) walk 128 x BN output tiles (BN = 256, or 128 when the wide tiles
+// would leave SMs idle), M-blocks fastest so the x tiles of a weight block are reused from L2.
+// Per 64-deep K block of a tile:
 //   * a TMA producer warp loads the x tile (128 x 64 bf16, 128-byte swizzle = the UMMA K-major
-//     canonical layout), 8 packed rows x 256 columns of codes and 2 rows of scales into a ring
-//     of its own (the B tiles below have a separate, shorter ring);
-//   * 16 dequant warps (two threads per weight column, one per group of the k-block) turn each
-//     packed word (8 consecutive k of one column) into 8 bf16 values: (w >> 4j) & 0x000F000F | 0x43004300 is the bf16 pair
-//     (128 + n_j, 128 + n_{j+4}); a bf16 FMA subtracts 136 exactly, another multiplies by the
-//     bf16 group scale; byte permutes restore k order; one 16-byte store puts them in the
-//     swizzled K-major B tile;
-//   * one thread issues 4 tcgen05.mma (M=128, N=256, K=16, bf16 x bf16 -> f32) into a TMEM
-//     accumulator and commits to the stage's "empty" barrier;
-//   * 4 epilogue warps drain the finished accumulator (double-buffered, 2 x 256 TMEM columns)
+//     canonical layout), 8 packed rows x BN columns of codes and 2 rows of scales into a 5-stage
+//     ring;
+//   * dequant warps (two threads per weight column, one per group of the k-block) turn each
+//     packed word (8 consecutive k of one column) into 8 bf16 values:
+//     ((w >> 4j) & 0x000F000F) | 0x43004300 is the bf16 pair (128 + n_j, 128 + n_{j+4}); a bf16
+//     FMA subtracts 136 exactly, another multiplies by the bf16 group scale; byte permutes
+//     restore k order; one 16-byte store puts them in the swizzled K-major B tile of a separate
+//     2-stage ring;
+//   * one thread issues 4 tcgen05.mma (M = 128, N = BN, K = 16, bf16 x bf16 -> f32) into a TMEM
+//     accumulator and commits to the barriers that free the x/codes stage and the B tile;
+//   * 4 epilogue warps drain the finished accumulator (double-buffered, 2 x BN TMEM columns)
 //     with tcgen05.ld, round to bf16 and store.
 // Every barrier wait is bounded; a timeout sets the device error word and the CTA winds down.
 #include <cuda_bf16.h>
@@ -47,7 +49,8 @@ constexpr int kDeqWarp0 = 6;
 #ifndef W4A16_PREFILL_DEQ_SPLIT
 #define W4A16_PREFILL_DEQ_SPLIT 2
 #endif
-constexpr int kDeqSplit = W4A16_PREFILL_DEQ_SPLIT;  // threads per weight column (groups per k-block split)
+// threads per weight column (each takes one group of the 64-deep k-block when 2)
+constexpr int kDeqSplit = W4A16_PREFILL_DEQ_SPLIT;
 static_assert(kDeqSplit == 1 || kDeqSplit == 2, "a 64-deep k-block holds two groups");
 // Everything that depends on the tile width BN (weight columns per tile: 256, or 128 when 256-wide
 // tiles would leave SMs idle).
@@ -176,8 +179,10 @@ __global__ void __launch_bounds__(PF<BN>::kThreads, 1)
           }
           mbar_expect_tx(bar(C::kFull + s), C::kStageTx);
           tma_load_3d(sb + C::kAOff + s * C::kABytes, &tmx, kb * BK, mb * BM, 0, bar(C::kFull + s));
-          tma_load_3d(sb + C::kQOff + s * C::kQBytes, &tmq, nb * BN, kb * (BK / 8), 0, bar(C::kFull + s));
-          tma_load_3d(sb + C::kSOff + s * C::kSBytes, &tms, nb * BN, kb * (BK / 32), 0, bar(C::kFull + s));
+          tma_load_3d(sb + C::kQOff + s * C::kQBytes, &tmq, nb * BN, kb * (BK / 8), 0,
+                      bar(C::kFull + s));
+          tma_load_3d(sb + C::kSOff + s * C::kSBytes, &tms, nb * BN, kb * (BK / 32), 0,
+                      bar(C::kFull + s));
         }
       }
       // Let the last copies land before the CTA can exit (they target this CTA's memory).
@@ -291,11 +296,12 @@ __global__ void __launch_bounds__(PF<BN>::kThreads, 1)
               uint32_t o[4];
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 hv = __floats2bfloat162_rn(__uint_as_float(r[8 * j + 2 * e]),
-                                                                __uint_as_float(r[8 * j + 2 * e + 1]));
+                const __nv_bfloat162 hv = __floats2bfloat162_rn(
+                    __uint_as_float(r[8 * j + 2 * e]), __uint_as_float(r[8 * j + 2 * e + 1]));
                 o[e] = *reinterpret_cast<const uint32_t*>(&hv);
               }
-              *reinterpret_cast<uint4*>(y + (size_t)row * N + col) = make_uint4(o[0], o[1], o[2], o[3]);
+              *reinterpret_cast<uint4*>(y + (size_t)row * N + col) =
+                  make_uint4(o[0], o[1], o[2], o[3]);
             }
           }
         }

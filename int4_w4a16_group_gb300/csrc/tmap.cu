@@ -92,7 +92,8 @@ cudaError_t make_tmap_ex(CUtensorMap* out, CUtensorMapDataType dtype, uint32_t e
 // kind 0: packed codes (int32, 128-byte swizzle); kind 1: scales (float32, no swizzle).
 cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t d2, uint32_t b0, uint32_t b1) {
-  return make_tmap_ex(out, kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+  return make_tmap_ex(out,
+                      kind == 0 ? CU_TENSOR_MAP_DATA_TYPE_INT32 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
                       4, kind == 0 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, base,
                       d0, d1, d2, b0, b1);
 }
