@@ -103,6 +103,27 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   return true;
 }
 
+// As mbar_wait, but polls with try_wait without a sleep hint (the hardware's own short
+// suspend), for hand-offs between warps of one CTA that recur every few hundred nanoseconds.
+__device__ __forceinline__ bool mbar_try_wait_poll(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait_poll(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_poll(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+
 // TMA tile copy of a 3-D tensor into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             int z, uint32_t bar) {
