@@ -14,7 +14,7 @@
 #include "internal.h"
 
 #ifndef W4A16_B16_STREAM_MAX_M
-#define W4A16_B16_STREAM_MAX_M 32
+#define W4A16_B16_STREAM_MAX_M 16
 #endif
 
 namespace w4a16 {

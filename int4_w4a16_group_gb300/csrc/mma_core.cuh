@@ -124,6 +124,62 @@ __device__ __forceinline__ bool mbar_wait_poll(uint32_t bar, uint32_t parity, ui
   return true;
 }
 
+// Cluster forms: this CTA's rank, the cluster address of a shared variable in CTA `rank`, an
+// arrive on a (possibly remote) barrier with cluster-scope release, a polled wait with
+// cluster-scope acquire (for barriers that other CTAs' threads arrive on), and a full cluster
+// barrier.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;\n" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr)
+               : "memory");
+}
+// Release of this CTA's shared-memory writes at cluster scope (cheaper than a full release: only
+// shared::cta accesses are ordered), to pair with mbar_arrive_remote_relaxed.
+__device__ __forceinline__ void fence_release_shared_cluster() {
+  asm volatile("fence.release.sync_restrict::shared::cta.cluster;\n" ::: "memory");
+}
+// Acquire counterpart: later accesses to the cluster's shared memory are ordered after a
+// completed barrier wait.
+__device__ __forceinline__ void fence_acquire_shared_cluster() {
+  asm volatile("fence.acquire.sync_restrict::shared::cluster.cluster;\n" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_addr) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(cluster_addr)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ bool mbar_wait_cluster(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (!mbar_try_wait_cluster(bar, parity)) {
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::
+                   : "memory");
+}
+
 // TMA tile copy of a 3-D tensor into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
                                             int z, uint32_t bar) {

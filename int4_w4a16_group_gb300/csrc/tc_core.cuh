@@ -38,14 +38,24 @@ __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, 
       "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// D (TMEM) [+]= A (TMEM: row i in lane i, two consecutive k per 32-bit column) * B (shared
-// memory).
-__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
-                                       uint32_t idesc, uint32_t accumulate) {
+// Pair form (cta_group::2, issued by one thread of the even CTA of a 2-CTA cluster): M = 256,
+// A rows 0-127 from this CTA's shared memory and rows 128-255 from the peer's at the same
+// address, B split in halves along N the same way; each CTA's TMEM holds its 128 rows of D.
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+      " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrives once on the mbarrier at offset `bar` in every CTA of `mask` when the pair MMAs issued
+// so far by this thread have completed.
+__device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t mask) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+      " [%0], %1;\n" ::"r"(bar),
+      "h"(mask)
       : "memory");
 }
 // Arrives once on the mbarrier when every MMA issued so far by this thread has completed.
@@ -108,20 +118,17 @@ __device__ __forceinline__ void tmem_wait_ld(uint32_t (&r)[32]) {
                :
                : "memory");
 }
-// Warp-collective TMEM store: thread l of warp w writes lane 32 (w % 4) + l, 16 consecutive
-// 32-bit columns starting at the address's column.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
-      "%13,%14,%15,%16};\n" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
+// TMEM allocation for a CTA pair: one warp of each CTA executes it; each CTA gets the base
+// address in its own shared memory at `dst`.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t cols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst),
+               "r"(cols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
 }
-// Waits until this thread's earlier tcgen05.st have completed.
-__device__ __forceinline__ void tmem_wait_st() {
-  asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory");
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t base, uint32_t cols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(base), "r"(cols)
+               : "memory");
 }
 }  // namespace tc
 }  // namespace w4a16

@@ -28,12 +28,13 @@ def _as_f64(t):
     return t.float().cpu().numpy().astype(np.float64)
 
 
-# 128-column tiles while twice the 256-column tile count fits in one wave (all but the last shape
-# here); (2440, 2056, 128) has 20 x 9 = 180 256-column tiles, so it runs the 256-column form with
-# a ragged last M block and N tile.
+# Tiles of 256 weight columns (128 per CTA of a pair) x up to 256 rows: (130, 264, 128) has a
+# second column tile the odd CTA sees only as zero fill, (48, 776, 320) a 48-row tile split 24/24
+# between the CTAs, and (2440, 2056, 128) 10 x 9 = 90 tiles, more than one per pair on any GPU,
+# with ragged last rows and columns.
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (1, 256, 64), (130, 264, 128),
                                    (300, 520, 192), (512, 1024, 1024), (48, 776, 320),
-                                   (2440, 2056, 128)])
+                                   (17, 264, 64), (2440, 2056, 128)])
 def test_prefill_small(w4, M, N, K):
     bits = synth.bf16_activations(M, K, seed=M + N)
     W = synth.weights(K, N, seed=K + N)
