@@ -23,9 +23,11 @@
 //     ((w >> 4j) & 0x000F000F) | 0x43004300 is the bf16 pair (128 + n_j, 128 + n_{j+4}); a bf16
 //     FMA subtracts 136 exactly, another multiplies by the bf16 group scale; byte permutes
 //     restore k order; one 16-byte store per word writes the swizzled K-major weight tile. Then
-//     they arrive on the even CTA's wready: locally, or, from the odd CTA, after a release of
-//     its shared-memory writes at cluster scope (the shared-memory-restricted fence; a full
-//     cluster-scope release costs about a microsecond per arrive);
+//     they arrive on the even CTA's wready, or, in the odd CTA, on a local barrier that one relay
+//     thread forwards: it releases the CTA's shared-memory writes at cluster scope (the
+//     shared-memory-restricted fence) and arrives remotely on wready (a full cluster-scope
+//     release costs about a microsecond, and even the restricted one is cheaper paid once per
+//     stage than by each of 8 warps);
 //   * one thread of the even CTA waits for wready alone (it follows both CTAs' full, which follow
 //     consumed), issues 4 pair MMAs (M = 256, N = tm, K = 16, bf16 x bf16 -> f32) into a TMEM
 //     accumulator and commits once to consumed in both CTAs;
@@ -63,7 +65,8 @@ constexpr int kProdWarp = 4;
 constexpr int kMmaWarp = 5;
 constexpr int kDeqWarp0 = 6;
 constexpr int kDeqWarps = 2 * TN / 32;  // two threads per weight column
-constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;
+constexpr int kRelayWarp = kDeqWarp0 + kDeqWarps;  // odd CTA: forwards dequant completion
+constexpr int kThreads = (kRelayWarp + 1) * 32;
 constexpr int kAccCols = TM;
 constexpr int kTmemCols = 2 * kAccCols;
 
@@ -71,10 +74,11 @@ constexpr int kWBytes = TN * BK * 2;
 constexpr int kQBytes = (BK / 8) * TN * 4;
 constexpr int kSBytes = (BK / 32) * TN * 4;
 constexpr int kBarOff = kRingBytes;
-// barriers: full[8] | wready[8] | consumed[8] | accfull[2] | accempty[2] | drain (wready,
-// accempty and drain are used in the even CTA only)
+// barriers: full[8] | wready[8] | consumed[8] | pready[8] | accfull[2] | accempty[2] | drain
+// (wready, accempty and drain are used in the even CTA only, pready in the odd CTA only)
 constexpr int kFull = 0, kWReady = kMaxStages, kConsumed = 2 * kMaxStages,
-              kAccFull = 3 * kMaxStages, kAccEmpty = kAccFull + 2, kDrain = kAccEmpty + 2;
+              kPReady = 3 * kMaxStages, kAccFull = 4 * kMaxStages, kAccEmpty = kAccFull + 2,
+              kDrain = kAccEmpty + 2;
 constexpr int kNumBars = kDrain + 1;
 constexpr int kMiscOff = kBarOff + kNumBars * 8;  // [0] TMEM base, [1] abort flag
 constexpr int kSmemBytes = kMiscOff + 16;
@@ -161,7 +165,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kMaxStages; ++s) {
       mbar_init(bar(kFull + s), 1);
-      mbar_init(bar(kWReady + s), 2 * kDeqWarps);  // both CTAs' dequant warps (even CTA)
+      mbar_init(bar(kWReady + s), kDeqWarps + 1);  // even CTA's dequant warps + the relay
+      mbar_init(bar(kPReady + s), kDeqWarps);      // odd CTA's dequant warps
       mbar_init(bar(kConsumed + s), 1);
     }
     for (int b = 0; b < 2; ++b) {
@@ -209,6 +214,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = (it > ns ? it - ns : 0); j < it; ++j)
         (void)mbar_wait(bar(kFull + j % ns), (j / ns) & 1, kWaitLimitNs / 16);
     }
+  } else if (warp == kRelayWarp) {
+    // Odd CTA: one thread waits for the local dequant barrier of each stage, releases the CTA's
+    // shared-memory writes at cluster scope and arrives on the even CTA's wready. One thread per
+    // CTA pays for the release instead of each of the 8 dequant warps.
+    if (rank == 1 && lane == 0) {
+      RingPos r;
+      bool ok = true;
+      for (int tile = cid; tile < tiles && ok && !aborted(); tile += nclusters) {
+        for (int kb = 0; kb < kblocks; ++kb, r.next(ns)) {
+          if (!PF_WAIT(bar(kPReady + r.s), r.ph, kWaitLimitNs) || aborted()) {
+            fail();
+            ok = false;
+            break;
+          }
+          fence_release_shared_cluster();
+          mbar_arrive_remote_relaxed(mapa_shared(bar(kWReady + r.s), 0));
+        }
+      }
+    }
   } else if (warp >= kDeqWarp0) {
     // Thread = weight column n of this CTA's 128 and scale group h of the 64-deep k-block (words
     // 4h .. 4h + 3).
@@ -243,12 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc::fence_proxy_async();  // make the generic-proxy stores visible to the tensor cores
         __syncwarp();
         if (lane == 0) {
-          if (rank == 0) {
-            tc::mbar_arrive(bar(kWReady + r.s));
-          } else {
-            fence_release_shared_cluster();
-            mbar_arrive_remote_relaxed(mapa_shared(bar(kWReady + r.s), 0));
-          }
+          tc::mbar_arrive(bar((rank == 0 ? kWReady : kPReady) + r.s));
         }
       }
     }
