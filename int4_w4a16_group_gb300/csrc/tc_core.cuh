@@ -1,6 +1,6 @@
 // 5th-generation tensor core (tcgen05) helpers: shared-memory matrix descriptors, MMA issue and
-// commit, Tensor Memory (TMEM) allocation and loads, and the fences that order them against
-// mbarrier hand-offs between warps.
+// commit for a CTA pair, Tensor Memory (TMEM) allocation and loads, and the fences that order
+// them against mbarrier hand-offs between warps.
 #pragma once
 #include <stdint.h>
 
@@ -29,15 +29,6 @@ constexpr uint32_t idesc_f16(bool bf16, int M, int N) {
          ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
-// D (TMEM) [+]= A (shared memory) * B (shared memory).
-__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
-  asm volatile(
-      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
-      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate)
-      : "memory");
-}
 // Pair form (cta_group::2, issued by one thread of the even CTA of a 2-CTA cluster): M = 256,
 // A rows 0-127 from this CTA's shared memory and rows 128-255 from the peer's at the same
 // address, B split in halves along N the same way; each CTA's TMEM holds its 128 rows of D.
@@ -58,12 +49,6 @@ __device__ __forceinline__ void commit_pair(uint32_t bar, uint16_t mask) {
       "h"(mask)
       : "memory");
 }
-// Arrives once on the mbarrier when every MMA issued so far by this thread has completed.
-__device__ __forceinline__ void commit(uint32_t bar) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
-      : "memory");
-}
 __device__ __forceinline__ void fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory");
 }
@@ -77,18 +62,6 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
 // tensor-core operand reads).
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
-}
-
-// TMEM allocation by one full warp; the base address is written to shared memory at `dst`.
-__device__ __forceinline__ void tmem_alloc(uint32_t dst, uint32_t cols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst),
-               "r"(cols)
-               : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
-}
-__device__ __forceinline__ void tmem_dealloc(uint32_t base, uint32_t cols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(base), "r"(cols)
-               : "memory");
 }
 
 // Warp-collective TMEM load: thread l of warp w reads lane 32 (w % 4) + l, 32 consecutive
