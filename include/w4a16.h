@@ -237,6 +237,13 @@ w4a16_status w4a16_bundle_load(w4a16_registry* reg, const char* path, void* aren
  * status in *code (W4A16_OK if none) and clears it. */
 w4a16_status w4a16_device_error(int* code);
 
+/* Self-test of that path: one thread waits on a shared-memory barrier with the kernels' own
+ * polled, time-limited wait. arrive = 0: nothing arrives, the wait gives up after limit_us
+ * microseconds (1 .. 100000, else W4A16_ERR_ARG) and records W4A16_ERR_TIMEOUT in the device
+ * error word; arrive = 1: the thread arrives first and nothing is recorded. Asynchronous on
+ * `stream`; read the outcome with w4a16_device_error. */
+w4a16_status w4a16_selftest_wait(int arrive, int limit_us, w4a16_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

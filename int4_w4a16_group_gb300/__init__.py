@@ -10,7 +10,7 @@ _EXPORTS = (
     "w4a16_dequantize",
     "w4a16_device_error", "w4a16_gemm", "w4a16_gemm_bf16", "w4a16_gemm_swiglu",
     "w4a16_load_qw_sc", "w4a16_moe_block", "w4a16_moe_block_workspace_size", "w4a16_moe_gemm",
-    "w4a16_moe_gemm_noalloc", "w4a16_moe_workspace_size", "w4a16_quantize",
+    "w4a16_moe_gemm_noalloc", "w4a16_moe_workspace_size", "w4a16_quantize", "w4a16_selftest_wait",
     "w4a16_status_string", "w4a16_topk_softmax",
 )
 

@@ -54,6 +54,7 @@ _SIGS = {
     "w4a16_linear": (_i, [_p, _s, _p, _p, _i, _p]),
     "w4a16_linear_swiglu": (_i, [_p, _s, _p, _p, _i, _p]),
     "w4a16_device_error": (_i, [ctypes.POINTER(_i)]),
+    "w4a16_selftest_wait": (_i, [_i, _i, _p]),
 }
 
 for _name, (_res, _args) in _SIGS.items():
@@ -292,6 +293,12 @@ def w4a16_device_error() -> int:
     code = ctypes.c_int(0)
     _check(_lib.w4a16_device_error(ctypes.byref(code)), "w4a16_device_error")
     return code.value
+
+
+def w4a16_selftest_wait(arrive: bool, limit_us: int, stream=None) -> None:
+    """Bounded-wait self-test kernel (see w4a16.h); read the result with w4a16_device_error()."""
+    _check(_lib.w4a16_selftest_wait(int(bool(arrive)), int(limit_us), _stream(stream)),
+           "w4a16_selftest_wait")
 
 
 def bundle_info(path: str):
