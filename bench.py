@@ -440,7 +440,7 @@ def other_workloads(args, w4, peaks, stream):
     res["moe_block_T64_E384_top8_shared"] = {
         "us": us, "active_experts": active, "algorithmic_bytes": mbs,
         "GB/s": mbs / (us * 1e-6) / 1e9, "frac_of_hbm": mbs / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
-        "launches_per_call": 4 + 2 * ((T + 15) // 16)}
+        "launches_per_call": 6}  # routing, 2 grouped passes, combine + shared gate/up, down
     del gq, gs, dq, ds, ws, sgq, sgs, sdq, sds
 
     # large-M bf16 contraction (tensor cores)

@@ -84,7 +84,7 @@ w4a16_status w4a16_dequantize(const int32_t* qw, const float* sc, int K, int N, 
  * Inference Engine", section "The Multi-Step Integration Chain", step 1; page "The Weight of
  * Precision ...", section "The Kernel: w4a16_gemm".
  * Any M >= 0; the kernels are built for the decode / draft-tree-verify regime (M <= 16):
- * larger M runs as consecutive 16-row slices. Deterministic (fixed reduction order). */
+ * larger M runs as 16-row slices within one launch. Deterministic (fixed reduction order). */
 w4a16_status w4a16_gemm(const float* x, const int32_t* qw, const float* sc, float* y,
                         int M, int N, int K, int group, w4a16_stream_t stream);
 
@@ -142,8 +142,8 @@ w4a16_status w4a16_moe_gemm(const float* x, const int32_t* topk_ids, const float
  *   qs_dn [Is/8, K] int32,   ss_dn [Is/32, K] float32
  * Other arguments as w4a16_moe_gemm; Is a multiple of 32; the shared expert's weights 16-byte
  * aligned. `workspace` holds at least w4a16_moe_block_workspace_size(T, topk, E, K, I, Is) bytes.
- * The shared expert runs as dense small-M GEMMs in 16-row slices; its output seeds each row of the
- * combine, which then adds the routed rows in slot order. Deterministic. */
+ * The shared expert runs as two dense small-M GEMMs (16-row slices in one launch each); its output
+ * seeds each row of the combine, which then adds the routed rows in slot order. Deterministic. */
 size_t w4a16_moe_block_workspace_size(int T, int topk, int E, int K, int I, int Is);
 w4a16_status w4a16_moe_block(const float* x, const int32_t* topk_ids, const float* topk_w,
                              int T, int topk, int E,

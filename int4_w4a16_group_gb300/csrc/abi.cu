@@ -115,8 +115,8 @@ w4a16_status gemm_impl(const float* x, const int32_t* qw, const float* sc, float
   if (!x || !y) return W4A16_ERR_ARG;
   if (!aligned16(x) || !aligned16(y)) return W4A16_ERR_ALIGN;
   const int n_out = swiglu ? N / 2 : N;
-  for (int r = 0; r < M; r += kGemvMaxM) {
-    const int rows = (M - r) < kGemvMaxM ? (M - r) : kGemvMaxM;
+  for (int r = 0; r < M; r += kGemvMaxRowsPerLaunch) {
+    const int rows = (M - r) < kGemvMaxRowsPerLaunch ? (M - r) : kGemvMaxRowsPerLaunch;
     cudaError_t e = launch_gemv(x + (size_t)r * K, qw, sc, y + (size_t)r * n_out, rows, N, K,
                                 swiglu, stream);
     if (e != cudaSuccess) return cuda_status(e);

@@ -55,6 +55,13 @@ using CodesGeo = Geo<NB, CH, kWN, W4A16_CODES_RING, NB == 1 ? 12288 : 16384>;
 template <int CH>
 using ActsGeo = Geo<4, CH, kWN, W4A16_ACTS_RING, 16384>;
 
+// Grid z = 16-row slices of a larger M (x and y advance by 16 rows per slice): the first row of
+// this CTA's slice and the slice's row count.
+__device__ __forceinline__ size_t slice_row0() { return (size_t)blockIdx.z * kGemvMaxM; }
+__device__ __forceinline__ int slice_rows(int M) {
+  return min(M - (int)blockIdx.z * kGemvMaxM, kGemvMaxM);
+}
+
 template <int NB, int CH, bool SWIGLU>
 __global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
     gemv_codes_kernel(const __grid_constant__ CUtensorMap tq,
@@ -63,6 +70,9 @@ __global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
   using L = CodesGeo<NB, CH>;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = align1024(smem_raw);
+  x += slice_row0() * K;
+  y += slice_row0() * (SWIGLU ? N / 2 : N);
+  M = slice_rows(M);
   cg::cluster_group cluster = cg::this_cluster();
   const int tile = blockIdx.x;
   const int CK = (int)cluster.dim_blocks().y;
@@ -105,6 +115,9 @@ __global__ void __launch_bounds__(kWN * 32, W4A16_ACTS_MINB)
   using L = ActsGeo<CH>;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = align1024(smem_raw);
+  x += slice_row0() * K;
+  y += slice_row0() * (SWIGLU ? N / 2 : N);
+  M = slice_rows(M);
   cg::cluster_group cluster = cg::this_cluster();
   const int tile = blockIdx.x;
   const int CK = (int)cluster.dim_blocks().y;
@@ -168,6 +181,9 @@ __global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
   using L = CodesGeo<NB, CH>;
   extern __shared__ __align__(1024) char smem_raw[];
   char* smem = align1024(smem_raw);
+  x += slice_row0() * K;  // M <= 16: one slice
+  y += slice_row0() * N;
+  M = slice_rows(M);
   cg::cluster_group cluster = cg::this_cluster();
   const int tile = blockIdx.x;
   const int CK = (int)cluster.dim_blocks().y;
@@ -244,6 +260,7 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
                          const int32_t* qw, const float* sc, YT* y, int M, int N, int K,
                          const DeviceInfo& di, cudaStream_t s) {
   const int G = K / kGroup;
+  const int nz = (M + kGemvMaxM - 1) / kGemvMaxM;  // 16-row slices, grid z
   const int bit = 1 << (di.device & 31);
   if (!(cache.device_mask & bit)) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -282,8 +299,8 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
     if (ck > 1 && G / ck < 8) break;
     const int nc = cache.max_clusters[ck];
     if (nc <= 0) continue;
-    const long long waves = (tiles + nc - 1) / nc;
-    const double eff = (double)tiles * ck / ((double)waves * slots);
+    const long long waves = ((long long)tiles * nz + nc - 1) / nc;
+    const double eff = (double)tiles * nz * ck / ((double)waves * slots);
     if (eff > best * 1.03) {
       best = eff;
       CK = ck;
@@ -295,7 +312,7 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
   e = make_tmap(&ts, 1, sc, (uint64_t)N, (uint64_t)(K / kGroup), 1, 32, kRows / 4);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles, CK, 1);
+  cfg.gridDim = dim3(tiles, CK, nz);
   cfg.blockDim = dim3(kWN * 32, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
@@ -338,7 +355,9 @@ long long fill_of(int N, int K) {
 }
 
 // Up to 4 rows: 4 tiles per warp (128 columns) when that still fills the GPU with CTAs (4 per
-// SM), else 2; 5..8 rows: 2; 9..16 rows: the activations-as-A kernel, 2 tiles.
+// SM), else 2; 5..8 rows: 2; 9 rows and more: the activations-as-A kernel, 2 tiles, one 16-row
+// slice per grid z (all slices in one launch, so CTAs of several slices stream the same weight
+// tiles at about the same time and share them through L2).
 template <bool SWIGLU>
 cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
                      int K, const DeviceInfo& di, cudaStream_t s) {
@@ -349,8 +368,7 @@ cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* 
     return wide ? launch_codes<1, W4A16_WIDE_CH, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
                 : launch_codes<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
   if (M <= 8) return launch_codes<2, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-  if (M <= 16) return launch_acts<2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-  return cudaErrorInvalidValue;
+  return launch_acts<2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);  // 9+ rows, 16 per grid z
 }
 
 template <int NB, int CH>

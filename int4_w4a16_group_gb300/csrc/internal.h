@@ -40,10 +40,12 @@ cudaError_t launch_dequantize(const int32_t* qw, const float* sc, int K, int N, 
                               cudaStream_t s);
 
 // ---- gemv.cu : small-M weight-streaming kernels.
-// Dense: y[M, N] = x[M, K] @ W.  SwiGLU: y[M, N/2] = silu(gate) * up.  M <= 16 per call.
+// Dense: y[M, N] = x[M, K] @ W.  SwiGLU: y[M, N/2] = silu(gate) * up.  Above 16 rows one launch
+// covers 16-row slices as grid z, so M <= kGemvMaxRowsPerLaunch per call.
 cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                         int N, int K, bool swiglu, cudaStream_t s);
 constexpr int kGemvMaxM = 16;
+constexpr int kGemvMaxRowsPerLaunch = kGemvMaxM * 4096;
 // The same for bf16 activations and bf16 output (y[M, N] = bf16(x @ W)), M <= 16.
 cudaError_t launch_gemv_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
                             int M, int N, int K, cudaStream_t s);

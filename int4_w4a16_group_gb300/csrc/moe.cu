@@ -277,7 +277,8 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
 
 // The routed experts as in launch_moe, plus (when qs_gu is given) a shared expert that every
 // token goes through with weight 1: its gate/up + SwiGLU and down projections run as dense
-// small-M GEMMs in 16-row slices into the workspace, and the combine starts each row from it.
+// small-M GEMMs (one launch each, 16-row slices as grid z) into the workspace, and the combine
+// starts each row from it.
 cudaError_t launch_moe_block(const float* x, const int32_t* ids, const float* w, int T, int topk,
                              int E, const int32_t* qw_gu, const float* sc_gu,
                              const int32_t* qw_dn, const float* sc_dn, const int32_t* qs_gu,
@@ -334,8 +335,8 @@ cudaError_t launch_moe_block(const float* x, const int32_t* ids, const float* w,
   if (qs_gu) {
     float* hs = reinterpret_cast<float*>(base + L.total);
     ys = reinterpret_cast<float*>(base + L.total + align256((size_t)T * Is * sizeof(float)));
-    for (int m0 = 0; m0 < T; m0 += kGemvMaxM) {
-      const int mc = T - m0 < kGemvMaxM ? T - m0 : kGemvMaxM;
+    for (int m0 = 0; m0 < T; m0 += kGemvMaxRowsPerLaunch) {
+      const int mc = T - m0 < kGemvMaxRowsPerLaunch ? T - m0 : kGemvMaxRowsPerLaunch;
       if ((e = launch_gemv(x + (size_t)m0 * K, qs_gu, ss_gu, hs + (size_t)m0 * Is, mc, 2 * Is, K,
                            true, s)) != cudaSuccess)
         return e;

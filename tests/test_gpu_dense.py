@@ -48,7 +48,7 @@ def test_dequantize_bit_exact_every_nibble(w4):
 
 # ----------------------------------------------------------------------------- GEMM
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 33])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 33, 100])
 @pytest.mark.parametrize("K,N", [(512, 1000), (2048, 260)])
 def test_gemm_small(w4, M, K, N):
     W = synth.weights(K, N, seed=M + K, outliers=True)
@@ -105,7 +105,7 @@ def test_gemm_is_deterministic(w4):
 
 # ----------------------------------------------------------------------------- SwiGLU
 
-@pytest.mark.parametrize("M", [1, 2, 4, 7, 16, 20])
+@pytest.mark.parametrize("M", [1, 2, 4, 7, 16, 20, 64])
 @pytest.mark.parametrize("K,I", [(1024, 520), (256, 64)])
 def test_swiglu_small(w4, M, K, I):
     W = synth.weights(K, 2 * I, seed=M + I)
