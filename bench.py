@@ -461,6 +461,23 @@ def other_workloads(args, w4, peaks, stream):
     except Exception as ex:  # the bf16 kernel may be unavailable in this build
         res["prefill_M4096_K7168_N18432"] = {"unavailable": str(ex).splitlines()[0]}
 
+    # Yardstick only (not this library's path): cuBLAS on the same shape with unquantized bf16
+    # weights, i.e. what a dense bf16 layer of this size costs on the same GPU.
+    try:
+        xb = synth.cuda_bf16_activations(M, K, seed=3)
+        wd = torch.randn((K, N), device="cuda", dtype=torch.bfloat16)
+        yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        fns = [lambda: torch.matmul(xb, wd, out=yb) for _ in range(reps + 3)]
+        t = _time_launches(stream, fns)[3:]
+        us = 1e3 * statistics.mean(t)
+        tf = 2.0 * M * N * K / (us * 1e-6) / 1e12
+        res["yardstick_cublas_bf16_dense_M4096_K7168_N18432"] = {
+            "us": us, "TFLOP/s": tf, "frac_of_bf16": tf / peaks["bf16_tflops"]}
+        del wd
+    except Exception as ex:
+        res["yardstick_cublas_bf16_dense_M4096_K7168_N18432"] = {
+            "unavailable": str(ex).splitlines()[0]}
+
     # bf16 activations at small M (K=7168, N=18432, bf16 in and out), 4 rotating weight copies
     K, N = synth.PREFILL["K"], synth.PREFILL["N"]
     wb = BYTES_PER_WEIGHT * K * N
