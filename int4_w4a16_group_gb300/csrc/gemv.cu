@@ -241,11 +241,11 @@ __global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
 
 constexpr int kMaxCluster = 16;
 
-struct LaunchCache {
-  int device_mask = 0;
-  int occ = 0;
-  int max_clusters[kMaxCluster + 1] = {0};  // index = cluster size
+struct LaunchData {
+  int occ;
+  int max_clusters[kMaxCluster + 1];  // index = cluster size
 };
+using LaunchCache = PerDeviceOnce<LaunchData>;
 
 // Slices (one warp each) of a problem for CH tiles per warp.
 template <int CH, bool SWIGLU>
@@ -261,16 +261,16 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
                          const DeviceInfo& di, cudaStream_t s) {
   const int G = K / kGroup;
   const int nz = (M + kGemvMaxM - 1) / kGemvMaxM;  // 16-row slices, grid z
-  const int bit = 1 << (di.device & 31);
-  if (!(cache.device_mask & bit)) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return e;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
+  const LaunchData* ld = nullptr;
+  cudaError_t e = cache.get(di.device, [&](LaunchData& d) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (r != cudaSuccess) return r;
+    r = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (r != cudaSuccess) return r;
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWN * 32, smem);
-    if (e != cudaSuccess) return e;
-    cache.occ = occ < 1 ? 1 : occ;
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWN * 32, smem);
+    if (r != cudaSuccess) return r;
+    d.occ = occ < 1 ? 1 : occ;
     for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1, ck, 1);
@@ -288,16 +288,17 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
         (void)cudaGetLastError();
         nc = 0;
       }
-      cache.max_clusters[ck] = nc;
+      d.max_clusters[ck] = nc;
     }
-    cache.device_mask |= bit;
-  }
-  const double slots = (double)di.sm_count * cache.occ;
+    return cudaSuccess;
+  }, &ld);
+  if (e != cudaSuccess) return e;
+  const double slots = (double)di.sm_count * ld->occ;
   int CK = 1;
   double best = -1.0;
   for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
     if (ck > 1 && G / ck < 8) break;
-    const int nc = cache.max_clusters[ck];
+    const int nc = ld->max_clusters[ck];
     if (nc <= 0) continue;
     const long long waves = ((long long)tiles * nz + nc - 1) / nc;
     const double eff = (double)tiles * nz * ck / ((double)waves * slots);
@@ -307,7 +308,7 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
     }
   }
   CUtensorMap tq, ts;
-  cudaError_t e = make_tmap(&tq, 0, qw, (uint64_t)N, (uint64_t)(K / 8), 1, 32, kRows);
+  e = make_tmap(&tq, 0, qw, (uint64_t)N, (uint64_t)(K / 8), 1, 32, kRows);
   if (e != cudaSuccess) return e;
   e = make_tmap(&ts, 1, sc, (uint64_t)N, (uint64_t)(K / kGroup), 1, 32, kRows / 4);
   if (e != cudaSuccess) return e;

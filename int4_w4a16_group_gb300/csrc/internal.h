@@ -6,6 +6,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <atomic>
+#include <mutex>
+
 namespace w4a16 {
 
 constexpr int kGroup = 32;
@@ -23,6 +26,32 @@ cudaError_t device_info(DeviceInfo* out);
 
 // Device address of the library's error word (one per device, lazily resolved).
 unsigned int* device_error_word();
+
+// Launch data a launcher computes once per device (kernel attributes set, occupancy queried).
+// Host threads may race to the first launch: the first one on a device runs `init` under the
+// lock and publishes the device's ready bit with release order, so a thread that sees the bit
+// (acquire) also sees the finished data.
+template <typename T>
+struct PerDeviceOnce {
+  std::atomic<uint32_t> ready{0};
+  std::mutex lock;
+  T data[32] = {};
+  template <typename Init>
+  cudaError_t get(int device, Init&& init, const T** out) {
+    const int d = device & 31;
+    const uint32_t bit = 1u << d;
+    if (!(ready.load(std::memory_order_acquire) & bit)) {
+      std::lock_guard<std::mutex> guard(lock);
+      if (!(ready.load(std::memory_order_relaxed) & bit)) {
+        const cudaError_t e = init(data[d]);
+        if (e != cudaSuccess) return e;
+        ready.fetch_or(bit, std::memory_order_release);
+      }
+    }
+    *out = &data[d];
+    return cudaSuccess;
+  }
+};
 
 // ---- tmap.cu : TMA descriptor of a row-major [d2][d1][d0] tensor of 4-byte elements, box
 // (b0 x b1 x 1); kind 0 = packed codes (int32, 128-byte swizzle), 1 = scales (float32).

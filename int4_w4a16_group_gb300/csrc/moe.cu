@@ -233,26 +233,28 @@ constexpr int kMoeSmem =
 template <bool SWIGLU>
 cudaError_t launch_grouped(const GroupedArgs& a, const int32_t* qw, const float* sc, int E,
                            const DeviceInfo& di, cudaStream_t s) {
-  static int occ_cache[64] = {0};
+  static PerDeviceOnce<int> occ_cache;  // resident CTAs per SM
   auto kern = moe_grouped_kernel<SWIGLU>;
-  int& occ = occ_cache[di.device & 63];
-  if (occ == 0) {
-    cudaError_t e =
+  const int* occ = nullptr;
+  cudaError_t e = occ_cache.get(di.device, [&](int& o) {
+    cudaError_t r =
         cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoeSmem);
-    if (e != cudaSuccess) return e;
-    int o = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kern, kWN * 32, kMoeSmem);
-    if (e != cudaSuccess) return e;
-    occ = o < 1 ? 1 : o;
-  }
+    if (r != cudaSuccess) return r;
+    int n = 0;
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWN * 32, kMoeSmem);
+    if (r != cudaSuccess) return r;
+    o = n < 1 ? 1 : n;
+    return cudaSuccess;
+  }, &occ);
+  if (e != cudaSuccess) return e;
   CUtensorMap tq, ts;
-  cudaError_t e = make_tmap(&tq, 0, qw, (uint64_t)a.N, (uint64_t)(a.Kr / 8), (uint64_t)E, 32,
+  e = make_tmap(&tq, 0, qw, (uint64_t)a.N, (uint64_t)(a.Kr / 8), (uint64_t)E, 32,
                             kRows);
   if (e != cudaSuccess) return e;
   e = make_tmap(&ts, 1, sc, (uint64_t)a.N, (uint64_t)(a.Kr / kGroup), (uint64_t)E, 32,
                 kRows / 4);
   if (e != cudaSuccess) return e;
-  kern<<<di.sm_count * occ, kWN * 32, kMoeSmem, s>>>(tq, ts, a);
+  kern<<<di.sm_count * *occ, kWN * 32, kMoeSmem, s>>>(tq, ts, a);
   return cudaGetLastError();
 }
 

@@ -361,12 +361,12 @@ cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* 
   DeviceInfo di;
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return e;
-  static int attr_devices = 0, max_pairs[32] = {0};
-  const int dev = di.device & 31, bit = 1 << dev;
-  if (!(attr_devices & bit)) {
-    e = cudaFuncSetAttribute(prefill_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             kSmemAlloc);
-    if (e != cudaSuccess) return e;
+  static PerDeviceOnce<int> pairs_cache;  // resident CTA pairs
+  const int* max_pairs = nullptr;
+  e = pairs_cache.get(di.device, [&](int& pairs) {
+    cudaError_t r = cudaFuncSetAttribute(prefill_pair_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemAlloc);
+    if (r != cudaSuccess) return r;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kThreads, 1, 1);
@@ -383,9 +383,10 @@ cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* 
       (void)cudaGetLastError();
       nc = 0;
     }
-    max_pairs[dev] = nc > 0 ? nc : di.sm_count / 2;
-    attr_devices |= bit;
-  }
+    pairs = nc > 0 ? nc : di.sm_count / 2;
+    return cudaSuccess;
+  }, &max_pairs);
+  if (e != cudaSuccess) return e;
   const int mblocks = (M + TM - 1) / TM;
   const int tm = (((M + mblocks - 1) / mblocks) + 15) / 16 * 16;
   CUtensorMap tmx, tmq, tms;
@@ -399,7 +400,7 @@ cudaError_t launch_gemm_bf16(const uint16_t* x, const int32_t* qw, const float* 
                    (uint64_t)N, (uint64_t)(K / kGroup), 1, TN, BK / 32);
   if (e != cudaSuccess) return e;
   const int tiles = mblocks * ((N + 2 * TN - 1) / (2 * TN));
-  const int pairs = tiles < max_pairs[dev] ? tiles : max_pairs[dev];
+  const int pairs = tiles < *max_pairs ? tiles : *max_pairs;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   cfg.blockDim = dim3(kThreads, 1, 1);
