@@ -113,3 +113,27 @@ def test_bf16_small_m_deterministic(w4):
     xd, qd, sd = _bf16_dev(bits), dev(qo), dev(so)
     np.testing.assert_array_equal(_as_f64(w4.w4a16_gemm_bf16(xd, qd, sd)),
                                   _as_f64(w4.w4a16_gemm_bf16(xd, qd, sd)))
+
+
+def test_prefill_repeatable_under_load(w4):
+    """The CTA-pair pipeline hands every stage across SMs through barriers (TMA completion, the
+    odd CTA's release relayed to the even CTA, the MMA commit multicast to both): a missed
+    ordering would show up as a changed bit somewhere in repeated full-size runs."""
+    c = synth.PREFILL
+    M, K, N = c["M"], c["K"], c["N"]
+    Wd = synth.cuda_weights(K, N, seed=3200)
+    qw, sc = w4.w4a16_quantize(Wd)
+    del Wd
+    xb = synth.cuda_bf16_activations(M, K, seed=32)
+    first = w4.w4a16_gemm_bf16(xb, qw, sc)
+    y = torch.empty_like(first)
+    for _ in range(40):
+        w4.w4a16_gemm_bf16(xb, qw, sc, y)
+        assert torch.equal(y.view(torch.int16), first.view(torch.int16))
+    xs = synth.cuda_bf16_activations(48, K, seed=33)
+    first = w4.w4a16_gemm_bf16(xs, qw, sc)
+    ys = torch.empty_like(first)
+    for _ in range(200):
+        w4.w4a16_gemm_bf16(xs, qw, sc, ys)
+        assert torch.equal(ys.view(torch.int16), first.view(torch.int16))
+    assert w4.w4a16_device_error() == 0
