@@ -155,11 +155,17 @@ _TRAFFIC_SOURCES = ("gemv.cu", "mma_core.cuh", "splitk.cuh", "internal.h")
 
 
 def _kernel_source_hash() -> str:
+    """Hash of those sources with comments and blank space removed (a comment edit does not
+    change the kernel the record was taken from)."""
+    import re
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "int4_w4a16_group_gb300", "csrc")
     for f in _TRAFFIC_SOURCES:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            code = re.sub(r"/\*.*?\*/", "", fh.read(), flags=re.S)
+        code = re.sub(r"//[^\n]*", "", code)
+        code = "\n".join(ln.strip() for ln in code.splitlines() if ln.strip())
+        h.update(f.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -7,8 +7,9 @@
 // design goal is to stream every packed weight and scale byte exactly once.
 //
 // Grid: x = tiles of kWN slices (one warp per slice of 32 or 64 weight columns), y = CK slices
-// of K. The CK CTAs of one tile form a thread-block cluster and add their partial tiles through
-// distributed shared memory in rank order: deterministic, no global scratch, no atomics.
+// of K, z = 16-row slices of M (one for M <= 16). The CK CTAs of one tile form a thread-block
+// cluster and add their partial tiles through distributed shared memory in rank order:
+// deterministic, no global scratch, no atomics.
 // The per-warp main loop lives in mma_core.cuh.
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
