@@ -609,6 +609,14 @@ def profile_case(name: str):
             y = torch.empty((M, N // 2 if name == "gate_up" else N), device="cuda")
             t = _time_launches(stream, [lambda: fn(x, qw, sc, y, stream=stream)] * 3)
             out[f"M{M}_us"] = 1e3 * t[-1]
+    elif name == "bf16_small":
+        K, N = synth.PREFILL["K"], synth.PREFILL["N"]
+        (qw, sc), = _quantized_copies(w4, K, N, 1, seed=5000)
+        for M in M_LIST:
+            xb = synth.cuda_bf16_activations(M, K, seed=M)
+            yb = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+            t = _time_launches(stream, [lambda: w4.w4a16_gemm_bf16(xb, qw, sc, yb, stream=stream)] * 3)
+            out[f"M{M}_us"] = 1e3 * t[-1]
     elif name == "prefill":
         M, K, N = 2048, synth.PREFILL["K"], synth.PREFILL["N"]
         (qw, sc), = _quantized_copies(w4, K, N, 1, seed=6000)
@@ -651,7 +659,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--copies", type=int, default=N_COPIES,
                     help="rotating weight copies of the headline workload (L2 defeat)")
-    ap.add_argument("--profile-case", choices=["gate_up", "down", "moe", "prefill"],
+    ap.add_argument("--profile-case", choices=["gate_up", "down", "moe", "prefill", "bf16_small"],
                     help="run one workload at ncu-capture size and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:
