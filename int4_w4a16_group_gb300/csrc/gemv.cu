@@ -254,16 +254,12 @@ int slices_of(int N) {
   return SWIGLU ? ((N >> 1) + 16 * CH - 1) / (16 * CH) : (N + 32 * CH - 1) / (32 * CH);
 }
 
-// Launches `kern` over tiles x CK clusters, CK chosen so that the waves of clusters fill the GPU
-// most evenly (each CTA keeps at least 8 groups of K).
-template <typename Kern, typename XT, typename YT>
-cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, const XT* x,
-                         const int32_t* qw, const float* sc, YT* y, int M, int N, int K,
-                         const DeviceInfo& di, cudaStream_t s) {
-  const int G = K / kGroup;
-  const int nz = (M + kGemvMaxM - 1) / kGemvMaxM;  // 16-row slices, grid z
-  const LaunchData* ld = nullptr;
-  cudaError_t e = cache.get(di.device, [&](LaunchData& d) {
+// A kernel's resident CTAs per SM and, per cluster size, its resident clusters (queried once per
+// device).
+template <typename Kern>
+cudaError_t launch_data(Kern kern, int smem, LaunchCache& cache, const DeviceInfo& di,
+                        const LaunchData** out) {
+  return cache.get(di.device, [&](LaunchData& d) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (r != cudaSuccess) return r;
     r = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -292,22 +288,42 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
       d.max_clusters[ck] = nc;
     }
     return cudaSuccess;
-  }, &ld);
-  if (e != cudaSuccess) return e;
-  const double slots = (double)di.sm_count * ld->occ;
+  }, out);
+}
+
+// Split-K factor for `units` clusters' worth of tiles (x row slices): the CK whose waves of
+// resident clusters fill the GPU's CTA slots most evenly, each CTA keeping at least 8 groups of K.
+// *eff = the filled fraction of the slots over those waves.
+inline int plan_split(const LaunchData& ld, long long units, int G, const DeviceInfo& di,
+                      double* eff) {
+  const double slots = (double)di.sm_count * ld.occ;
   int CK = 1;
   double best = -1.0;
   for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
     if (ck > 1 && G / ck < 8) break;
-    const int nc = ld->max_clusters[ck];
+    const int nc = ld.max_clusters[ck];
     if (nc <= 0) continue;
-    const long long waves = ((long long)tiles * nz + nc - 1) / nc;
-    const double eff = (double)tiles * nz * ck / ((double)waves * slots);
-    if (eff > best * 1.03) {
-      best = eff;
+    const long long waves = (units + nc - 1) / nc;
+    const double e = (double)units * ck / ((double)waves * slots);
+    if (e > best * 1.03) {
+      best = e;
       CK = ck;
     }
   }
+  if (eff) *eff = best;
+  return CK;
+}
+
+// Launches `kern` over tiles x CK clusters x 16-row slices of M.
+template <typename Kern, typename XT, typename YT>
+cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, const XT* x,
+                         const int32_t* qw, const float* sc, YT* y, int M, int N, int K,
+                         const DeviceInfo& di, cudaStream_t s) {
+  const int nz = (M + kGemvMaxM - 1) / kGemvMaxM;  // 16-row slices, grid z
+  const LaunchData* ld = nullptr;
+  cudaError_t e = launch_data(kern, smem, cache, di, &ld);
+  if (e != cudaSuccess) return e;
+  const int CK = plan_split(*ld, (long long)tiles * nz, K / kGroup, di, nullptr);
   CUtensorMap tq, ts;
   e = make_tmap(&tq, 0, qw, (uint64_t)N, (uint64_t)(K / 8), 1, 32, kRows);
   if (e != cudaSuccess) return e;
@@ -328,47 +344,67 @@ cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, con
   return cudaLaunchKernelEx(&cfg, kern, tq, ts, x, y, M, N, K, device_error_word());
 }
 
+// One launch cache per kernel instantiation.
+template <int NB, int CH, bool SWIGLU>
+LaunchCache codes_cache;
+template <int CH, bool SWIGLU>
+LaunchCache acts_cache;
+template <int NB, int CH>
+LaunchCache b16_cache;
+
 template <int NB, int CH, bool SWIGLU>
 cudaError_t launch_codes(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                          int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  static LaunchCache cache;
   const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
-  return launch_split(gemv_codes_kernel<NB, CH, SWIGLU>, CodesGeo<NB, CH>::kAlloc, cache, tiles,
-                      x, qw, sc, y, M, N, K, di, s);
+  return launch_split(gemv_codes_kernel<NB, CH, SWIGLU>, CodesGeo<NB, CH>::kAlloc,
+                      codes_cache<NB, CH, SWIGLU>, tiles, x, qw, sc, y, M, N, K, di, s);
 }
 
 template <int CH, bool SWIGLU>
 cudaError_t launch_acts(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                         int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  static LaunchCache cache;
   const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
-  return launch_split(gemv_acts_kernel<CH, SWIGLU>, ActsGeo<CH>::kAlloc, cache, tiles, x, qw, sc,
-                      y, M, N, K, di, s);
+  return launch_split(gemv_acts_kernel<CH, SWIGLU>, ActsGeo<CH>::kAlloc, acts_cache<CH, SWIGLU>,
+                      tiles, x, qw, sc, y, M, N, K, di, s);
 }
 
-// CTAs a problem can occupy with CH tiles per warp: column tiles times the largest split that
-// still leaves each CTA 8 groups of K (at most a 16-CTA cluster).
-template <int CH, bool SWIGLU>
-long long fill_of(int N, int K) {
-  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
-  int ck = 1;
-  while (ck < kMaxCluster && (K / kGroup) / (2 * ck) >= 8) ck *= 2;
-  return (long long)tiles * ck;
+// Whether 4 tiles per warp (128 columns) fill the GPU at least about as well as 2: each width's
+// tiles with the split-K factor its resident clusters allow (plan_split). Wide tiles halve the
+// CTAs but share each activation fragment between more columns, so they win ties.
+template <typename KernW, typename KernN>
+cudaError_t prefer_wide(KernW kw, int smem_w, LaunchCache& cw, int tiles_w, KernN kn, int smem_n,
+                        LaunchCache& cn, int tiles_n, int K, const DeviceInfo& di, bool* wide) {
+  const LaunchData *lw = nullptr, *ln = nullptr;
+  cudaError_t e = launch_data(kw, smem_w, cw, di, &lw);
+  if (e != cudaSuccess) return e;
+  e = launch_data(kn, smem_n, cn, di, &ln);
+  if (e != cudaSuccess) return e;
+  double ew = 0.0, en = 0.0;
+  (void)plan_split(*lw, tiles_w, K / kGroup, di, &ew);
+  (void)plan_split(*ln, tiles_n, K / kGroup, di, &en);
+  *wide = ew * 1.03 >= en;
+  return cudaSuccess;
 }
 
-// Up to 4 rows: 4 tiles per warp (128 columns) when that still fills the GPU with CTAs (4 per
-// SM), else 2; 5..8 rows: 2; 9 rows and more: the activations-as-A kernel, 2 tiles, one 16-row
-// slice per grid z (all slices in one launch, so CTAs of several slices stream the same weight
-// tiles at about the same time and share them through L2).
+// Up to 4 rows: 4 or 2 tiles per warp (prefer_wide); 5..8 rows: 2; 9 rows and more: the
+// activations-as-A kernel, 2 tiles, one 16-row slice per grid z (all slices in one launch, so CTAs
+// of several slices stream the same weight tiles at about the same time and share them through
+// L2).
 template <bool SWIGLU>
 cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
                      int K, const DeviceInfo& di, cudaStream_t s) {
-  const long long slots = 4LL * di.sm_count;
-  const bool wide = fill_of<W4A16_WIDE_CH, SWIGLU>(N, K) * 10 >= slots * 8 ||
-                    fill_of<W4A16_WIDE_CH, SWIGLU>(N, K) >= fill_of<2, SWIGLU>(N, K);
-  if (M <= 4)
-    return wide ? launch_codes<1, W4A16_WIDE_CH, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
+  if (M <= 4) {
+    constexpr int W = W4A16_WIDE_CH;
+    bool wide = true;
+    const cudaError_t e = prefer_wide(
+        gemv_codes_kernel<1, W, SWIGLU>, CodesGeo<1, W>::kAlloc, codes_cache<1, W, SWIGLU>,
+        (slices_of<W, SWIGLU>(N) + kWN - 1) / kWN, gemv_codes_kernel<1, 2, SWIGLU>,
+        CodesGeo<1, 2>::kAlloc, codes_cache<1, 2, SWIGLU>,
+        (slices_of<2, SWIGLU>(N) + kWN - 1) / kWN, K, di, &wide);
+    if (e != cudaSuccess) return e;
+    return wide ? launch_codes<1, W, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
                 : launch_codes<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+  }
   if (M <= 8) return launch_codes<2, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
   return launch_acts<2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);  // 9+ rows, 16 per grid z
 }
@@ -376,10 +412,9 @@ cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* 
 template <int NB, int CH>
 cudaError_t launch_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y, int M,
                        int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  static LaunchCache cache;
   const int tiles = (slices_of<CH, false>(N) + kWN - 1) / kWN;
-  return launch_split(gemv_b16_kernel<NB, CH>, CodesGeo<NB, CH>::kAlloc, cache, tiles, x, qw, sc,
-                      y, M, N, K, di, s);
+  return launch_split(gemv_b16_kernel<NB, CH>, CodesGeo<NB, CH>::kAlloc, b16_cache<NB, CH>, tiles,
+                      x, qw, sc, y, M, N, K, di, s);
 }
 
 }  // namespace
@@ -389,12 +424,17 @@ cudaError_t launch_gemv_b16(const uint16_t* x, const int32_t* qw, const float* s
   DeviceInfo di;
   cudaError_t e = device_info(&di);
   if (e != cudaSuccess) return e;
-  const long long slots = 4LL * di.sm_count;
-  const bool wide = fill_of<W4A16_B16_WIDE_CH, false>(N, K) * 10 >= slots * 8 ||
-                    fill_of<W4A16_B16_WIDE_CH, false>(N, K) >= fill_of<2, false>(N, K);
-  if (M <= 8)
-    return wide ? launch_b16<1, W4A16_B16_WIDE_CH>(x, qw, sc, y, M, N, K, di, s)
+  if (M <= 8) {
+    constexpr int W = W4A16_B16_WIDE_CH;
+    bool wide = true;
+    e = prefer_wide(gemv_b16_kernel<1, W>, CodesGeo<1, W>::kAlloc, b16_cache<1, W>,
+                    (slices_of<W, false>(N) + kWN - 1) / kWN, gemv_b16_kernel<1, 2>,
+                    CodesGeo<1, 2>::kAlloc, b16_cache<1, 2>,
+                    (slices_of<2, false>(N) + kWN - 1) / kWN, K, di, &wide);
+    if (e != cudaSuccess) return e;
+    return wide ? launch_b16<1, W>(x, qw, sc, y, M, N, K, di, s)
                 : launch_b16<1, 2>(x, qw, sc, y, M, N, K, di, s);
+  }
   if (M <= 16) return launch_b16<2, 2>(x, qw, sc, y, M, N, K, di, s);
   return cudaErrorInvalidValue;
 }
