@@ -31,10 +31,12 @@ def _as_f64(t):
 # Tiles of 256 weight columns (128 per CTA of a pair) x up to 256 rows: (130, 264, 128) has a
 # second column tile the odd CTA sees only as zero fill, (48, 776, 320) a 48-row tile split 24/24
 # between the CTAs, and (2440, 2056, 128) 10 x 9 = 90 tiles, more than one per pair on any GPU,
-# with ragged last rows and columns.
+# with ragged last rows and columns. (40, 8, 64) is a single 8-column tile; (4097, 264, 128) has
+# 17 row blocks of 256 whose last holds one row.
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (1, 256, 64), (130, 264, 128),
                                    (300, 520, 192), (512, 1024, 1024), (48, 776, 320),
-                                   (17, 264, 64), (2440, 2056, 128)])
+                                   (17, 264, 64), (2440, 2056, 128), (40, 8, 64),
+                                   (4097, 264, 128)])
 def test_prefill_small(w4, M, N, K):
     bits = synth.bf16_activations(M, K, seed=M + N)
     W = synth.weights(K, N, seed=K + N)
