@@ -142,3 +142,8 @@ def test_loader_rejects_missing_and_wrong_size(lib, tmp_path):
     assert lib.w4a16_load_qw_sc(str(qp).encode(), str(sp).encode(), K, N, 32, B, B) == 7
     np.zeros((K // 8, N), dtype=np.int32)[:-1].tofile(qp)            # truncated .qw
     assert lib.w4a16_load_qw_sc(str(qp).encode(), str(sp).encode(), K, N, 32, B, B) == 7
+
+
+@pytest.mark.parametrize("limit_us", [0, -5, 100001])
+def test_selftest_wait_limit_checked_before_any_cuda_call(lib, limit_us):
+    assert lib.w4a16_selftest_wait(0, limit_us, None) == 1  # W4A16_ERR_ARG
