@@ -160,12 +160,16 @@ w4a16_status w4a16_moe_block(const float* x, const int32_t* topk_ids, const floa
  * an addition of this library.
  *   - Arguments and results as w4a16_moe_gemm, without the workspace: the scratch is one array
  *     of W4A16_MOE_STATIC_SCRATCH_BYTES in device memory that the library's device code holds on
- *     every GPU that loads it, until the process exits. No allocation happens in the call.
- *   - Sizes with w4a16_moe_workspace_size(T, topk, E, K, I) > W4A16_MOE_STATIC_SCRATCH_BYTES
- *     are refused with W4A16_ERR_WORKSPACE before anything is launched (at K = 7168, I = 2048
- *     that allows up to 910 token-expert pairs, e.g. T = 64 tokens with top-8).
- *   - The first call on each device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *     every GPU that loads it, until the process exits or the device is reset. No allocation
+ *     happens in the call.
+ *   - The argument checks and their order are those of w4a16_moe_gemm; then sizes with
+ *     w4a16_moe_workspace_size(T, topk, E, K, I) > W4A16_MOE_STATIC_SCRATCH_BYTES are refused
+ *     with W4A16_ERR_WORKSPACE before anything is launched (at K = 7168, I = 2048 that allows
+ *     up to 909 token-expert pairs for any E <= 4096, e.g. T = 64 tokens with top-8).
+ *   - Each call outside stream capture looks up the array's device address (with the device
+ *     current), so a device reset, which releases the array, does not leave a stale address.
+ *     A call under stream capture reuses the last address looked up on that device: make one
+ *     call on the device before capturing (else W4A16_ERR_CUDA).
  *   - All calls on a device share the one array and it keeps whatever the last call left there
  *     (nothing in it needs to start at zero). Calls whose execution overlaps on the GPU -- on
  *     different streams, or from different host threads -- race on it; serialize them. */

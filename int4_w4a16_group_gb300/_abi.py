@@ -96,6 +96,11 @@ def _dev(t: torch.Tensor, dtype, name: str, shape=None) -> int:
         raise TypeError(f"{name}: expected a torch.Tensor")
     if not t.is_cuda:
         raise ValueError(f"{name}: must be a CUDA tensor")
+    if t.device.index != torch.cuda.current_device():
+        # the library launches on the current device: a tensor of another GPU would be read from
+        # the wrong device's address space
+        raise ValueError(f"{name}: on {t.device}, but the current CUDA device is "
+                         f"cuda:{torch.cuda.current_device()}")
     if t.dtype != dtype:
         raise TypeError(f"{name}: dtype {t.dtype}, expected {dtype}")
     if not t.is_contiguous():

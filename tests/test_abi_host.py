@@ -147,3 +147,29 @@ def test_loader_rejects_missing_and_wrong_size(lib, tmp_path):
 @pytest.mark.parametrize("limit_us", [0, -5, 100001])
 def test_selftest_wait_limit_checked_before_any_cuda_call(lib, limit_us):
     assert lib.w4a16_selftest_wait(0, limit_us, None) == 1  # W4A16_ERR_ARG
+
+
+def test_noalloc_scratch_bound_is_909_pairs(lib):
+    # The fixed scratch of w4a16_moe_gemm_noalloc holds the workspace of 909 token-expert pairs
+    # at K = 7168, I = 2048 for any expert count up to 4096, and not that of 910.
+    limit = 32 << 20
+    for E in (1, 64, 384, 4096):
+        assert lib.w4a16_moe_workspace_size(909, 1, E, 7168, 2048) <= limit
+        assert lib.w4a16_moe_workspace_size(910, 1, E, 7168, 2048) > limit
+        assert lib.w4a16_moe_workspace_size(64, 8, E, 7168, 2048) <= limit
+
+
+@pytest.mark.parametrize("T,topk,E,K,I,group,want", [
+    (4096, 8, 384, 7168, 2048, 64, 3),   # a bad group wins over a too-large size: UNSUPPORTED
+    (4096, 65, 384, 7168, 2048, 32, 1),  # topk > 64 -> ARG before the size check
+    (4096, 8, 5000, 7168, 2048, 32, 1),  # E > 4096 -> ARG
+    (4096, 8, 384, 7000, 2048, 32, 1),   # K % 32 != 0 -> ARG
+    (0, 8, 384, 7168, 2048, 32, 0),      # T == 0: nothing to do
+    (4096, 8, 384, 7168, 2048, 32, 4),   # valid arguments, scratch too small -> WORKSPACE
+])
+def test_noalloc_checks_arguments_like_the_workspace_entry(lib, T, topk, E, K, I, group, want):
+    st = lib.w4a16_moe_gemm_noalloc(A, A, A, T, topk, E, B, B, B, B, Y, K, I, group, None)
+    assert st == want
+    if want != 4:  # the workspace entry answers the same (with any workspace pointer)
+        st2 = lib.w4a16_moe_gemm(A, A, A, T, topk, E, B, B, B, B, Y, K, I, group, Y, 1 << 40, None)
+        assert st2 == want

@@ -13,8 +13,9 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import synth
-from gpu_util import FP32_TOL, assert_close_rows, host, lib
+from gpu_util import FP32_TOL, assert_close_rows, dev, host, lib
 
 pytestmark = pytest.mark.gpu
 
@@ -81,3 +82,59 @@ def test_noalloc_refuses_sizes_beyond_its_scratch(w4):
                                      K, I, 32, None)
     assert st == 4  # W4A16_ERR_WORKSPACE
     assert w4.w4a16_moe_workspace_size(64, 8, 384, 7168, 2048) <= limit
+
+
+def test_noalloc_matches_the_oracle(w4):
+    # Experts quantized by the oracle on the host; the no-alloc call against the oracle's MoE
+    # forward, every row.
+    T, E, topk, K, I, seed = 40, 12, 4, 256, 96, 3
+    gu, dn = zip(*[synth.moe_expert_weights(e, K, I, seed=seed) for e in range(E)])
+    gu_q = [oracle.quantize_w4a16(a) for a in gu]
+    dn_q = [oracle.quantize_w4a16(b) for b in dn]
+    ids, logits = synth.routing(T, E, topk, seed=seed)
+    x = synth.activations(T, K, seed=seed)
+    ref = oracle.moe_forward(x, ids, oracle.topk_softmax(logits), gu_q.__getitem__,
+                             dn_q.__getitem__)
+    prob = (dev(x), dev(ids), w4.w4a16_topk_softmax(dev(logits)),
+            dev(np.stack([q for q, _ in gu_q])), dev(np.stack([s for _, s in gu_q])),
+            dev(np.stack([q for q, _ in dn_q])), dev(np.stack([s for _, s in dn_q])))
+    out = torch.full((T, K), float("nan"), device="cuda")
+    assert _call_noalloc(w4, prob, out) == 0
+    assert_close_rows(host(out), ref, FP32_TOL, "no-alloc vs oracle")
+    assert w4.w4a16_device_error() == 0
+
+
+def test_noalloc_at_its_pair_limit(w4):
+    # 909 token-expert pairs at K = 7168, I = 2048: the largest problem the fixed scratch holds.
+    # Two experts of full size (each streamed once per 8-row pass); the result equals the
+    # workspace entry's bit for bit, and three sampled tokens match the oracle, which quantizes
+    # their experts from the same float32 weights.
+    T, topk, E, K, I, seed = 909, 1, 2, 7168, 2048, 4
+    assert w4.w4a16_moe_workspace_size(T, topk, E, K, I) <= 32 << 20
+    assert w4.w4a16_moe_workspace_size(T + 1, topk, E, K, I) > 32 << 20
+    gq = torch.empty((E, K // 8, 2 * I), dtype=torch.int32, device="cuda")
+    gs = torch.empty((E, K // 32, 2 * I), dtype=torch.float32, device="cuda")
+    dq = torch.empty((E, I // 8, K), dtype=torch.int32, device="cuda")
+    ds = torch.empty((E, I // 32, K), dtype=torch.float32, device="cuda")
+    for e in range(E):
+        a, b = synth.cuda_moe_expert_weights(e, K, I, seed=seed)
+        w4.w4a16_quantize(a, gq[e], gs[e])
+        w4.w4a16_quantize(b, dq[e], ds[e])
+    del a, b
+    ids, logits = synth.routing(T, E, topk, seed=seed)
+    x = synth.activations(T, K, seed=seed)
+    prob = (dev(x), dev(ids), w4.w4a16_topk_softmax(dev(logits)), gq, gs, dq, ds)
+    out = torch.full((T, K), float("nan"), device="cuda")
+    assert _call_noalloc(w4, prob, out) == 0
+    got = host(out)
+    np.testing.assert_array_equal(got, host(w4.w4a16_moe_gemm(*prob)))
+    assert w4.w4a16_device_error() == 0
+    toks = [0, T // 2, T - 1]
+    gu_o, dn_o = {}, {}
+    for e in sorted(set(int(ids[t, 0]) for t in toks)):
+        a, b = synth.cuda_moe_expert_weights(e, K, I, seed=seed)
+        gu_o[e] = oracle.quantize_w4a16(host(a))
+        dn_o[e] = oracle.quantize_w4a16(host(b))
+    ref = oracle.moe_forward(x[toks], ids[toks], oracle.topk_softmax(logits[toks]),
+                             gu_o.__getitem__, dn_o.__getitem__)
+    assert_close_rows(got[toks], ref, FP32_TOL, "no-alloc at 909 pairs")
