@@ -22,7 +22,6 @@ namespace w4a16 {
 namespace {
 thread_local int g_last_cuda_error = 0;
 
-constexpr int kMaxDevices = 64;
 DeviceInfo g_info[kMaxDevices];
 bool g_info_valid[kMaxDevices];
 std::mutex g_info_mutex;

@@ -31,15 +31,20 @@ unsigned int* device_error_word();
 // Host threads may race to the first launch: the first one on a device runs `init` under the
 // lock and publishes the device's ready bit with release order, so a thread that sees the bit
 // (acquire) also sees the finished data.
+// Devices 0 .. kMaxDevices - 1 are served (the same bound as the rest of the library); a larger
+// id is refused with cudaErrorInvalidDevice.
+constexpr int kMaxDevices = 64;
+
 template <typename T>
 struct PerDeviceOnce {
-  std::atomic<uint32_t> ready{0};
+  std::atomic<uint64_t> ready{0};
   std::mutex lock;
-  T data[32] = {};
+  T data[kMaxDevices] = {};
   template <typename Init>
   cudaError_t get(int device, Init&& init, const T** out) {
-    const int d = device & 31;
-    const uint32_t bit = 1u << d;
+    if (device < 0 || device >= kMaxDevices) return cudaErrorInvalidDevice;
+    const int d = device;
+    const uint64_t bit = 1ull << d;
     if (!(ready.load(std::memory_order_acquire) & bit)) {
       std::lock_guard<std::mutex> guard(lock);
       if (!(ready.load(std::memory_order_relaxed) & bit)) {
@@ -62,6 +67,12 @@ cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0,
 cudaError_t make_tmap_ex(CUtensorMap* out, CUtensorMapDataType dtype, uint32_t elem_bytes,
                          CUtensorMapSwizzle swz, const void* base, uint64_t d0, uint64_t d1,
                          uint64_t d2, uint32_t b0, uint32_t b1);
+
+// Tiled descriptor of 2..5 dimensions: dims[0] contiguous, strides[i] = byte stride of
+// dimension i + 1 (any order), box per dimension. Out-of-range box elements read as zero.
+cudaError_t make_tmap_nd(CUtensorMap* out, CUtensorMapDataType dtype, CUtensorMapSwizzle swz,
+                         const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box);
 
 // ---- quant.cu
 cudaError_t launch_quantize(const float* W, int K, int N, int32_t* qw, float* sc, cudaStream_t s);

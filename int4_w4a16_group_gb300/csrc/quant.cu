@@ -62,24 +62,36 @@ __global__ void dequantize_kernel(const int32_t* __restrict__ qw, const float* _
   }
 }
 
-int grid_for(long long total, int block) {
+// Grid-stride launch size: one CTA per `block` items, at most 64 CTAs per SM of this device.
+cudaError_t grid_for(long long total, int block, int* grid) {
+  DeviceInfo di;
+  const cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
   long long b = (total + block - 1) / block;
-  if (b > 152LL * 64) b = 152LL * 64;
-  return (int)(b < 1 ? 1 : b);
+  const long long cap = (long long)di.sm_count * 64;
+  if (b > cap) b = cap;
+  *grid = (int)(b < 1 ? 1 : b);
+  return cudaSuccess;
 }
 
 }  // namespace
 
 cudaError_t launch_quantize(const float* W, int K, int N, int32_t* qw, float* sc, cudaStream_t s) {
   const long long total = (long long)(K / kGroup) * N;
-  quantize_kernel<<<grid_for(total, 256), 256, 0, s>>>(W, K, N, qw, sc);
+  int grid = 0;
+  const cudaError_t e = grid_for(total, 256, &grid);
+  if (e != cudaSuccess) return e;
+  quantize_kernel<<<grid, 256, 0, s>>>(W, K, N, qw, sc);
   return cudaGetLastError();
 }
 
 cudaError_t launch_dequantize(const int32_t* qw, const float* sc, int K, int N, float* W,
                               cudaStream_t s) {
   const long long total = (long long)(K / 8) * N;
-  dequantize_kernel<<<grid_for(total, 256), 256, 0, s>>>(qw, sc, K, N, W);
+  int grid = 0;
+  const cudaError_t e = grid_for(total, 256, &grid);
+  if (e != cudaSuccess) return e;
+  dequantize_kernel<<<grid, 256, 0, s>>>(qw, sc, K, N, W);
   return cudaGetLastError();
 }
 

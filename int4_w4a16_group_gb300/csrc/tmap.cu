@@ -89,6 +89,32 @@ cudaError_t make_tmap_ex(CUtensorMap* out, CUtensorMapDataType dtype, uint32_t e
   return cudaSuccess;
 }
 
+// Tiled descriptor of `rank` (2..5) dimensions with explicit byte strides of dimensions 1..rank-1
+// (any order: a dimension may step through memory faster than the one before it) and box
+// `box[0..rank-1]`. Out-of-range box elements read as zero. Not cached: callers build these once
+// per launch.
+cudaError_t make_tmap_nd(CUtensorMap* out, CUtensorMapDataType dtype, CUtensorMapSwizzle swz,
+                         const void* base, int rank, const uint64_t* dims,
+                         const uint64_t* strides, const uint32_t* box) {
+  if (rank < 2 || rank > 5) return cudaErrorInvalidValue;
+  std::call_once(g_encode_once, load_encode);
+  if (!g_encode) return g_encode_status;
+  cuuint64_t d[5], st[4];
+  cuuint32_t b[5], es[5];
+  for (int i = 0; i < rank; ++i) {
+    d[i] = dims[i];
+    b[i] = box[i];
+    es[i] = 1;
+    if (i > 0) st[i - 1] = strides[i - 1];
+  }
+  memset(out, 0, sizeof(*out));
+  const CUresult r = g_encode(out, dtype, (cuuint32_t)rank, const_cast<void*>(base), d, st, b, es,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // kind 0: packed codes (int32, 128-byte swizzle); kind 1: scales (float32, no swizzle).
 cudaError_t make_tmap(CUtensorMap* out, int kind, const void* base, uint64_t d0, uint64_t d1,
                       uint64_t d2, uint32_t b0, uint32_t b1) {
