@@ -1,277 +1,241 @@
 // Small-M (decode / draft-tree verify) weight-streaming GEMM: y = x @ dequant(W), float32
-// activations and output (also in a bf16 form: bf16 activations and output, M <= 16).
+// activations and output, optionally with the fused gate/up SwiGLU epilogue; and the bf16 form
+// (bf16 activations and output, M <= 16).
 //
 // Page "The Weight of Precision: Building Native INT4 Quantization for a Custom Speculative
 // Decoding Engine", section "The Kernel: w4a16_gemm" (FP32 activations, packed INT4 weights,
 // group-32 float32 scales); the pages measure the optimized kernel against HBM bandwidth, so the
-// design goal is to stream every packed weight and scale byte exactly once.
+// design goal is to stream every packed weight and scale byte exactly once with as few
+// instructions per weight as possible. The roles of a CTA live in stream.cuh.
 //
-// Grid: x = tiles of kWN slices (one warp per slice of 32 or 64 weight columns), y = CK slices
-// of K, z = 16-row slices of M (one for M <= 16). The CK CTAs of one tile form a thread-block
-// cluster and add their partial tiles through distributed shared memory in rank order:
-// deterministic, no global scratch, no atomics.
-// The per-warp main loop lives in mma_core.cuh.
+// Grid: x = CTA column tiles (W consumer warps x CH 32-column tiles each), y = CK ranks of a
+// split over K (one thread-block cluster; partial tiles are added over distributed shared
+// memory in rank order: deterministic, no global scratch, no atomics), z = row slices of the
+// activations (16 rows each; one slice for M <= 16).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "internal.h"
-#include "mma_core.cuh"
 #include "splitk.cuh"
+#include "stream.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace w4a16 {
 namespace {
 
-using namespace mma;
+using ws::Acc;
+using ws::LaneRows;
+using ws::WeightMaps;
 
-// Geometry of the two orientations.
-//   up to 8 rows : A = codes; 4-warp CTAs, 2-stage rings and a 12-16 KB activation budget keep
-//                  a CTA near 53 KB so four fit per SM (16 warps, ~80 KB of copies in flight);
-//   9..16 rows   : A = activations (no padded MMA rows); 4-warp CTAs, 3-stage rings, 16 KB.
-constexpr int kWN = 4;  // warps (slices) per CTA
+// Kernel geometries: WsGeo<mode, blocks, consumer warps, tiles per warp, groups per stage,
+// ring stages, groups per activation chunk, activation bytes>.
+//   up to 4 rows (two-term columns): 512 or 256 columns per CTA;
+//   5..8 rows and 9..16 rows (terms summed over k): 512 or 256 columns;
+//   bf16 activations (one term): 512 or 256 columns.
+// Compile-time knobs (consumer warps of the wide form, ring stages, chunk groups per mode); the
+// defaults are the measured best on GB300. The wide form has 16 tiles (512 columns) per CTA, the
+// narrow form 8 tiles with half the warps; both keep CH = 16 / W tiles per warp.
+#ifndef W4A16_N2_W
+#define W4A16_N2_W 4
+#endif
+#ifndef W4A16_N2_R
+#define W4A16_N2_R 4
+#endif
+#ifndef W4A16_K2A_W
+#define W4A16_K2A_W 4
+#endif
+#ifndef W4A16_K2A_R
+#define W4A16_K2A_R 4
+#endif
+#ifndef W4A16_K2B_W
+#define W4A16_K2B_W 4
+#endif
+#ifndef W4A16_K2B_R
+#define W4A16_K2B_R 3
+#endif
+#ifndef W4A16_K2B_CG
+#define W4A16_K2B_CG 4
+#endif
+#ifndef W4A16_B16_W
+#define W4A16_B16_W 4
+#endif
+#ifndef W4A16_B16_R
+#define W4A16_B16_R 4
+#endif
+#ifndef W4A16_MINB
+#define W4A16_MINB 2
+#endif
+// Launch with programmatic stream serialization: a launch may overlap the tail of the previous
+// kernel on its stream (only the activation loads wait for it).
+#ifndef W4A16_PDL
+#define W4A16_PDL 0
+#endif
+// Ring depth scales with 16 / (tiles per CTA), so the narrow form keeps the wide form's bytes in
+// flight per CTA.
+template <int W, int CH>
+using GeoN2 = ws::WsGeo<ws::kN2, 1, W, CH, 2, W4A16_N2_R * 16 / (W * CH), 8, 4>;
+template <int W, int CH>
+using GeoK2a = ws::WsGeo<ws::kK2, 1, W, CH, 2, W4A16_K2A_R * 16 / (W * CH), 8, 4>;
+template <int W, int CH>
+using GeoK2b = ws::WsGeo<ws::kK2, 2, W, CH, 2, W4A16_K2B_R * 16 / (W * CH), W4A16_K2B_CG, 4>;
+template <int NB, int W, int CH>
+using GeoB16 = ws::WsGeo<ws::kK1, NB, W, CH, 2, W4A16_B16_R * 16 / (W * CH), 8, 2>;
+constexpr int kN2W = W4A16_N2_W, kN2CH = 16 / W4A16_N2_W;
+constexpr int kK2aW = W4A16_K2A_W, kK2aCH = 16 / W4A16_K2A_W;
+constexpr int kK2bW = W4A16_K2B_W, kK2bCH = 16 / W4A16_K2B_W;
+constexpr int kB16W = W4A16_B16_W, kB16CH = 16 / W4A16_B16_W;
 
-// Tuning knobs (compile-time; defaults are the measured best on GB300).
-#ifndef W4A16_CODES_RING
-#define W4A16_CODES_RING 2
-#endif
-#ifndef W4A16_CODES_MINB
-#define W4A16_CODES_MINB 4
-#endif
-#ifndef W4A16_ACTS_RING
-#define W4A16_ACTS_RING 3
-#endif
-#ifndef W4A16_ACTS_MINB
-#define W4A16_ACTS_MINB 4
-#endif
-#ifndef W4A16_WIDE_CH
-#define W4A16_WIDE_CH 4
-#endif
-#ifndef W4A16_B16_WIDE_CH
-#define W4A16_B16_WIDE_CH 4
-#endif
-
-template <int NB, int CH>
-using CodesGeo = Geo<NB, CH, kWN, W4A16_CODES_RING, NB == 1 ? 12288 : 16384>;
-template <int CH>
-using ActsGeo = Geo<4, CH, kWN, W4A16_ACTS_RING, 16384>;
-
-// Grid z = 16-row slices of a larger M (x and y advance by 16 rows per slice): the first row of
-// this CTA's slice and the slice's row count.
-__device__ __forceinline__ size_t slice_row0() { return (size_t)blockIdx.z * kGemvMaxM; }
-__device__ __forceinline__ int slice_rows(int M) {
-  return min(M - (int)blockIdx.z * kGemvMaxM, kGemvMaxM);
+// Output element stores: float32, or bf16 (bit pattern in uint16_t) rounded to nearest even.
+__device__ __forceinline__ void store4(float* y, float4 v) { *reinterpret_cast<float4*>(y) = v; }
+__device__ __forceinline__ void store4(uint16_t* y, float4 v) {
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
+  uint2 o;
+  o.x = *reinterpret_cast<const uint32_t*>(&lo);
+  o.y = *reinterpret_cast<const uint32_t*>(&hi);
+  *reinterpret_cast<uint2*>(y) = o;
 }
 
-template <int NB, int CH, bool SWIGLU>
-__global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
-    gemv_codes_kernel(const __grid_constant__ CUtensorMap tq,
-                      const __grid_constant__ CUtensorMap ts, const float* __restrict__ x,
-                      float* __restrict__ y, int M, int N, int K, unsigned int* err) {
-  using L = CodesGeo<NB, CH>;
+__device__ __forceinline__ float4 swiglu4(float4 g, float4 u) {
+  return make_float4(mma::silu_f(g.x) * u.x, mma::silu_f(g.y) * u.y, mma::silu_f(g.z) * u.z,
+                     mma::silu_f(g.w) * u.w);
+}
+
+// Grid z = row slices of kRows rows: the slice's first row.
+template <typename L>
+__device__ __forceinline__ int slice_row0() {
+  return (int)blockIdx.z * L::MI::kRows;
+}
+
+template <typename L, bool SWIGLU, typename XT, typename YT>
+__global__ void __launch_bounds__(L::kThreads, W4A16_MINB)
+    ws_gemv_kernel(const __grid_constant__ WeightMaps wm, const __grid_constant__ CUtensorMap xmap,
+                   YT* __restrict__ y, int M, int N, int K, unsigned int* err) {
+  constexpr int MODE = L::kMode, NB = L::kNB, CH = L::kCH, G = L::kG;
+  using LR = LaneRows<MODE, NB>;
   extern __shared__ __align__(1024) char smem_raw[];
-  char* smem = align1024(smem_raw);
-  x += slice_row0() * K;
-  y += slice_row0() * (SWIGLU ? N / 2 : N);
-  M = slice_rows(M);
+  char* base = mma::align1024(smem_raw);
   cg::cluster_group cluster = cg::this_cluster();
-  const int tile = blockIdx.x;
-  const int CK = (int)cluster.dim_blocks().y;
-  const int rank = (int)cluster.block_index().y;
-  const int warp = threadIdx.x >> 5;
-  const int G = K / kGroup;
-  const int q0 = (int)((long long)rank * G / CK);
-  const int q1 = (int)((long long)(rank + 1) * G / CK);
-
-  init_barriers<L>(smem, kWN);
-  float acc[CH][2][NB][4];
-  int seq = 0;
-  auto rowptr = [&](int m) { return x + (size_t)m * K; };
-  stream_groups<NB, CH, SWIGLU, kWN, L>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN,
-                                        smem, seq, err, acc);
-  if (CK == 1) {
-    store_direct<NB, CH, SWIGLU>(acc, tile * kWN + warp, N, M, y);
-    return;
-  }
-  constexpr int kCols = kWN * 32 * CH;
-  static_assert(4 * NB * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
-                "split-K tile must fit in the code ring");
-  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-#pragma unroll
-  for (int c = 0; c < CH; ++c)
-#pragma unroll
-    for (int b = 0; b < NB; ++b)
-      *reinterpret_cast<float4*>(&red[(4 * b + t) * kCols +
-                                      tile_local_col<CH, SWIGLU, kWN>(warp, c, g)]) =
-          chunk_result<NB, CH>(acc, c, b);
-  cluster_finish<SWIGLU, kCols>(cluster, red, tile, M, N, y);
-}
-
-template <int CH, bool SWIGLU>
-__global__ void __launch_bounds__(kWN * 32, W4A16_ACTS_MINB)
-    gemv_acts_kernel(const __grid_constant__ CUtensorMap tq,
-                     const __grid_constant__ CUtensorMap ts, const float* __restrict__ x,
-                     float* __restrict__ y, int M, int N, int K, unsigned int* err) {
-  using L = ActsGeo<CH>;
-  extern __shared__ __align__(1024) char smem_raw[];
-  char* smem = align1024(smem_raw);
-  x += slice_row0() * K;
-  y += slice_row0() * (SWIGLU ? N / 2 : N);
-  M = slice_rows(M);
-  cg::cluster_group cluster = cg::this_cluster();
-  const int tile = blockIdx.x;
-  const int CK = (int)cluster.dim_blocks().y;
-  const int rank = (int)cluster.block_index().y;
-  const int warp = threadIdx.x >> 5;
-  const int G = K / kGroup;
-  const int q0 = (int)((long long)rank * G / CK);
-  const int q1 = (int)((long long)(rank + 1) * G / CK);
-
-  init_barriers<L>(smem, kWN);
-  float acc[CH][4][4];
-  int seq = 0;
-  auto rowptr = [&](int m) { return x + (size_t)m * K; };
-  stream_groups_xa<CH, SWIGLU, kWN, L>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN, smem,
-                                       seq, err, acc);
-  if (CK == 1) {
-    store_direct_xa<CH, SWIGLU>(acc, tile * kWN + warp, N, M, y);
-    return;
-  }
-  constexpr int kCols = kWN * 32 * CH;
-  static_assert(16 * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
-                "split-K tile must fit in the code ring");
-  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
-  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int hh[2] = {lane_chunk(2 * t), lane_chunk(2 * t + 1)};
-#pragma unroll
-  for (int c = 0; c < CH; ++c)
-#pragma unroll
-    for (int hf = 0; hf < 2; ++hf)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        // tile_local_col with the lane chunk of B column 2t + e
-        int lc;
-        if (SWIGLU) {
-          constexpr int H = CH / 2;
-          lc = (c >= H ? kWN * 16 * CH : 0) + warp * 16 * CH + 32 * (c >= H ? c - H : c) +
-               4 * hh[e];
-        } else {
-          lc = warp * 32 * CH + 32 * c + 4 * hh[e];
-        }
-        *reinterpret_cast<float4*>(&red[(g + 8 * hf) * kCols + lc]) = xa_result<CH>(acc, c, hf, e);
-      }
-  cluster_finish<SWIGLU, kCols>(cluster, red, tile, M, N, y);
-}
-
-// bf16 activations (x[M, K] bf16, y[M, N] bf16, M <= 16): the codes orientation with x rows as
-// MMA columns, 8 rows per n8 block. Lane (g, t) ends with rows 8b + 2t and 8b + 2t + 1 of n8 block
-// b; for each of them the lane's 4 columns 4 h(g) + 0..3 of tile c are below.
-template <int NB, int CH>
-__device__ __forceinline__ float4 b16_result(const float (&acc)[CH][2][NB][4], int c, int b,
-                                             int odd) {
-  return make_float4(acc[c][0][b][odd], acc[c][0][b][2 + odd], acc[c][1][b][odd],
-                     acc[c][1][b][2 + odd]);
-}
-
-template <int NB, int CH>
-__global__ void __launch_bounds__(kWN * 32, W4A16_CODES_MINB)
-    gemv_b16_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap ts,
-                    const uint16_t* __restrict__ x, uint16_t* __restrict__ y, int M, int N, int K,
-                    unsigned int* err) {
-  using L = CodesGeo<NB, CH>;
-  extern __shared__ __align__(1024) char smem_raw[];
-  char* smem = align1024(smem_raw);
-  x += slice_row0() * K;  // M <= 16: one slice
-  y += slice_row0() * N;
-  M = slice_rows(M);
-  cg::cluster_group cluster = cg::this_cluster();
-  const int tile = blockIdx.x;
   const int CK = (int)cluster.dim_blocks().y;
   const int rank = (int)cluster.block_index().y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int G = K / kGroup;
-  const int q0 = (int)((long long)rank * G / CK);
-  const int q1 = (int)((long long)(rank + 1) * G / CK);
+  const int xrow0 = slice_row0<L>();
+  const int Ms = min(M - xrow0, L::MI::kRows);
+  const int ldy = SWIGLU ? N / 2 : N;
+  y += (size_t)xrow0 * ldy;
+  // This rank's groups: whole stages of G groups, split as evenly as possible.
+  const int Gt = K / kGroup;
+  const int U = (Gt + G - 1) / G;
+  const int q0 = G * (int)((long long)rank * U / CK);
+  const int q1 = min(Gt, G * (int)((long long)(rank + 1) * U / CK));
+  const int nq = q1 - q0;
 
-  init_barriers<L>(smem, kWN);
-  float acc[CH][2][NB][4];
-  int seq = 0;
-  auto rowptr = [&](int m) { return x + (size_t)m * K; };
-  stream_groups<NB, CH, false, kWN, L, true>(rowptr, M, &tq, &ts, 0, N, q0, q1 - q0, tile * kWN,
-                                             smem, seq, err, acc);
+  ws::init_roles<L>(base);
+  if (threadIdx.x == 0) ws::allow_dependents();
+  __syncthreads();
+  Acc<CH, NB> acc;
+  int ex[LR::kN];
+  if (warp == 0) {
+    if (lane == 0) {
+      ws::prefetch_tmap(&wm.codes);
+      ws::prefetch_tmap(&wm.scales);
+      ws::producer_loop<SWIGLU, L>(wm, base, q0, nq, blockIdx.x, N, 0, err);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) ws::prefetch_tmap(&xmap);
+    ws::prep_loop<XT, L>(&xmap, base, q0, nq, xrow0, err);
+  } else {
+    ws::consumer_loop<SWIGLU, L>(base, nq, warp - 2, err, acc, ex);
+  }
+  __syncthreads();  // every role is done with the rings; the code ring becomes the reduction tile
+
+  const int w = warp - 2;
+  const int h4 = 4 * mma::lane_chunk(g);
+  constexpr int kT = L::kTiles;
   if (CK == 1) {
+    if (warp < 2) return;
 #pragma unroll
-    for (int c = 0; c < CH; ++c) {
-      bool valid;
-      const int col = out_col<CH, false>(tile * kWN + warp, c, g, N, &valid);
-      if (!valid) continue;
+    for (int i = 0; i < LR::kN; ++i) {
+      const int m = LR::row(t, i);
+      if (m >= Ms) continue;
+      const float f = mma::exp2i(ex[i] - 14);
+      const int b = MODE == ws::kN2 ? 0 : (i >> 1), odd = i & 1;
+      if constexpr (SWIGLU) {
+        constexpr int H = CH / 2;
 #pragma unroll
-      for (int b = 0; b < NB; ++b)
-#pragma unroll
-        for (int odd = 0; odd < 2; ++odd) {
-          const int m = 8 * b + 2 * t + odd;
-          if (m < M) {
-            const float4 v = b16_result<NB, CH>(acc, c, b, odd);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(v.x, v.y);
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(v.z, v.w);
-            uint2 o;
-            o.x = *reinterpret_cast<const uint32_t*>(&lo);
-            o.y = *reinterpret_cast<const uint32_t*>(&hi);
-            *reinterpret_cast<uint2*>(y + (size_t)m * N + col) = o;
-          }
+        for (int c = 0; c < H; ++c) {
+          const int j = 32 * (blockIdx.x * (kT / 2) + w * H + c) + h4;
+          if (j < ldy)
+            store4(y + (size_t)m * ldy + j,
+                   swiglu4(ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f),
+                           ws::lane_result<MODE, CH, NB>(acc, c + H, b, odd, f)));
         }
+      } else {
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int col = 32 * (blockIdx.x * kT + w * CH + c) + h4;
+          if (col < N)
+            store4(y + (size_t)m * N + col, ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f));
+        }
+      }
     }
     return;
   }
-  constexpr int kCols = kWN * 32 * CH;
-  static_assert(8 * NB * kCols * 4 <= kWN * L::kRing * CH * L::kCodeTile,
+  constexpr int kCols = kT * 32;
+  static_assert(L::MI::kRows * kCols * 4 <= L::kR * L::kCodeStage,
                 "split-K tile must fit in the code ring");
-  float* red = reinterpret_cast<float*>(smem + L::kCodeOff);
+  float* red = reinterpret_cast<float*>(base + L::kCodeOff);
+  if (warp >= 2) {
 #pragma unroll
-  for (int c = 0; c < CH; ++c)
+    for (int i = 0; i < LR::kN; ++i) {
+      const int m = LR::row(t, i);
+      if (m >= Ms) continue;
+      const float f = mma::exp2i(ex[i] - 14);
+      const int b = MODE == ws::kN2 ? 0 : (i >> 1), odd = i & 1;
 #pragma unroll
-    for (int b = 0; b < NB; ++b)
-#pragma unroll
-      for (int odd = 0; odd < 2; ++odd)
-        *reinterpret_cast<float4*>(&red[(8 * b + 2 * t + odd) * kCols +
-                                        tile_local_col<CH, false, kWN>(warp, c, g)]) =
-            b16_result<NB, CH>(acc, c, b, odd);
-  cluster_finish<false, kCols, uint16_t>(cluster, red, tile, M, N, y);
+      for (int c = 0; c < CH; ++c) {
+        int lc;
+        if constexpr (SWIGLU) {
+          constexpr int H = CH / 2;
+          lc = (c >= H ? kCols / 2 : 0) + 32 * (w * H + (c >= H ? c - H : c)) + h4;
+        } else {
+          lc = 32 * (w * CH + c) + h4;
+        }
+        *reinterpret_cast<float4*>(&red[m * kCols + lc]) =
+            ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f);
+      }
+    }
+  }
+  mma::cluster_finish<SWIGLU, kCols, YT>(cluster, red, blockIdx.x, Ms, N, y);
 }
+
+// ------------------------------------------------------------------------------ host side
 
 constexpr int kMaxCluster = 16;
 
 struct LaunchData {
-  int occ;
-  int max_clusters[kMaxCluster + 1];  // index = cluster size
+  int occ;                             // resident CTAs per SM
+  int max_clusters[kMaxCluster + 1];   // resident clusters per cluster size
 };
 using LaunchCache = PerDeviceOnce<LaunchData>;
 
-// Slices (one warp each) of a problem for CH tiles per warp.
-template <int CH, bool SWIGLU>
-int slices_of(int N) {
-  return SWIGLU ? ((N >> 1) + 16 * CH - 1) / (16 * CH) : (N + 32 * CH - 1) / (32 * CH);
-}
-
-// A kernel's resident CTAs per SM and, per cluster size, its resident clusters (queried once per
-// device).
 template <typename Kern>
-cudaError_t launch_data(Kern kern, int smem, LaunchCache& cache, const DeviceInfo& di,
-                        const LaunchData** out) {
+cudaError_t launch_data(Kern kern, int smem, int threads, LaunchCache& cache,
+                        const DeviceInfo& di, const LaunchData** out) {
   return cache.get(di.device, [&](LaunchData& d) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (r != cudaSuccess) return r;
     r = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (r != cudaSuccess) return r;
     int occ = 0;
-    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kWN * 32, smem);
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, smem);
     if (r != cudaSuccess) return r;
     d.occ = occ < 1 ? 1 : occ;
-    for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
+    for (int ck = 1; ck <= kMaxCluster; ++ck) {
       cudaLaunchConfig_t cfg = {};
       cfg.gridDim = dim3(1, ck, 1);
-      cfg.blockDim = dim3(kWN * 32, 1, 1);
+      cfg.blockDim = dim3(threads, 1, 1);
       cfg.dynamicSmemBytes = smem;
       cudaLaunchAttribute at[1];
       at[0].id = cudaLaunchAttributeClusterDimension;
@@ -291,21 +255,21 @@ cudaError_t launch_data(Kern kern, int smem, LaunchCache& cache, const DeviceInf
   }, out);
 }
 
-// Split-K factor for `units` clusters' worth of tiles (x row slices): the CK whose waves of
-// resident clusters fill the GPU's CTA slots most evenly, each CTA keeping at least 8 groups of K.
-// *eff = the filled fraction of the slots over those waves.
-inline int plan_split(const LaunchData& ld, long long units, int G, const DeviceInfo& di,
+// Split over K for `units` clusters (column tiles x row slices): the cluster size whose waves of
+// resident clusters fill the GPU's CTA slots best, each rank keeping at least two stages. *eff
+// receives the filled fraction of the slots over those waves.
+inline int plan_split(const LaunchData& ld, long long units, int stages, const DeviceInfo& di,
                       double* eff) {
   const double slots = (double)di.sm_count * ld.occ;
   int CK = 1;
   double best = -1.0;
-  for (int ck = 1; ck <= kMaxCluster; ck *= 2) {
-    if (ck > 1 && G / ck < 8) break;
+  for (int ck = 1; ck <= kMaxCluster; ++ck) {
+    if (ck > 1 && stages / ck < 2) break;
     const int nc = ld.max_clusters[ck];
     if (nc <= 0) continue;
     const long long waves = (units + nc - 1) / nc;
     const double e = (double)units * ck / ((double)waves * slots);
-    if (e > best * 1.03) {
+    if (e > best * 1.02) {
       best = e;
       CK = ck;
     }
@@ -314,130 +278,170 @@ inline int plan_split(const LaunchData& ld, long long units, int G, const Device
   return CK;
 }
 
-// Launches `kern` over tiles x CK clusters x 16-row slices of M.
-template <typename Kern, typename XT, typename YT>
-cudaError_t launch_split(Kern kern, int smem, LaunchCache& cache, int tiles, const XT* x,
-                         const int32_t* qw, const float* sc, YT* y, int M, int N, int K,
-                         const DeviceInfo& di, cudaStream_t s) {
-  const int nz = (M + kGemvMaxM - 1) / kGemvMaxM;  // 16-row slices, grid z
-  const LaunchData* ld = nullptr;
-  cudaError_t e = launch_data(kern, smem, cache, di, &ld);
-  if (e != cudaSuccess) return e;
-  const int CK = plan_split(*ld, (long long)tiles * nz, K / kGroup, di, nullptr);
-  CUtensorMap tq, ts;
-  e = make_tmap(&tq, 0, qw, (uint64_t)N, (uint64_t)(K / 8), 1, 32, kRows);
-  if (e != cudaSuccess) return e;
-  e = make_tmap(&ts, 1, sc, (uint64_t)N, (uint64_t)(K / kGroup), 1, 32, kRows / 4);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(tiles, CK, nz);
-  cfg.blockDim = dim3(kWN * 32, 1, 1);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = s;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 1;
-  attr[0].val.clusterDim.y = CK;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, ts, x, y, M, N, K, device_error_word());
+template <typename L, bool SWIGLU>
+int cta_tiles(int N) {
+  const int tiles = SWIGLU ? ((N >> 1) + 31) / 32 : (N + 31) / 32;
+  const int per = SWIGLU ? L::kTiles / 2 : L::kTiles;
+  return (tiles + per - 1) / per;
 }
 
-// One launch cache per kernel instantiation.
-template <int NB, int CH, bool SWIGLU>
-LaunchCache codes_cache;
-template <int CH, bool SWIGLU>
-LaunchCache acts_cache;
-template <int NB, int CH>
-LaunchCache b16_cache;
-
-template <int NB, int CH, bool SWIGLU>
-cudaError_t launch_codes(const float* x, const int32_t* qw, const float* sc, float* y, int M,
-                         int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
-  return launch_split(gemv_codes_kernel<NB, CH, SWIGLU>, CodesGeo<NB, CH>::kAlloc,
-                      codes_cache<NB, CH, SWIGLU>, tiles, x, qw, sc, y, M, N, K, di, s);
+// Weight descriptors of a [K, N] matrix for geometry L.
+template <typename L, bool SWIGLU>
+cudaError_t weight_maps(WeightMaps* wm, const int32_t* qw, const float* sc, int N, int K) {
+  constexpr int G = L::kG, kT = L::kTiles;
+  const uint64_t rows = (uint64_t)K / 8, grows = (uint64_t)K / kGroup, n = (uint64_t)N;
+  const bool fast = SWIGLU ? ((N / 2) % 32 == 0) : (N % 32 == 0);
+  wm->fast = fast ? 1 : 0;
+  cudaError_t e;
+  if (fast) {
+    if (SWIGLU) {
+      const uint64_t I = n / 2;
+      const uint64_t dq[5] = {32, rows, I / 32, 2, 1};
+      const uint64_t sq[4] = {n * 4, 128, I * 4, rows * n * 4};
+      const uint32_t bq[5] = {32, 4 * G, kT / 2, 2, 1};
+      e = make_tmap_nd(&wm->codes, CU_TENSOR_MAP_DATA_TYPE_INT32, CU_TENSOR_MAP_SWIZZLE_128B, qw,
+                       5, dq, sq, bq);
+      if (e != cudaSuccess) return e;
+      const uint64_t ds[5] = {32, grows, I / 32, 2, 1};
+      const uint64_t ss[4] = {n * 4, 128, I * 4, grows * n * 4};
+      const uint32_t bs[5] = {32, G, kT / 2, 2, 1};
+      return make_tmap_nd(&wm->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                          CU_TENSOR_MAP_SWIZZLE_NONE, sc, 5, ds, ss, bs);
+    }
+    const uint64_t dq[4] = {32, rows, n / 32, 1};
+    const uint64_t sq[3] = {n * 4, 128, rows * n * 4};
+    const uint32_t bq[4] = {32, 4 * G, kT, 1};
+    e = make_tmap_nd(&wm->codes, CU_TENSOR_MAP_DATA_TYPE_INT32, CU_TENSOR_MAP_SWIZZLE_128B, qw, 4,
+                     dq, sq, bq);
+    if (e != cudaSuccess) return e;
+    const uint64_t ds[4] = {32, grows, n / 32, 1};
+    const uint64_t ss[3] = {n * 4, 128, grows * n * 4};
+    const uint32_t bs[4] = {32, G, kT, 1};
+    return make_tmap_nd(&wm->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        sc, 4, ds, ss, bs);
+  }
+  const uint64_t dq[3] = {n, rows, 1};
+  const uint64_t sq[2] = {n * 4, rows * n * 4};
+  const uint32_t bq[3] = {32, 4 * G, 1};
+  e = make_tmap_nd(&wm->codes, CU_TENSOR_MAP_DATA_TYPE_INT32, CU_TENSOR_MAP_SWIZZLE_128B, qw, 3, dq,
+                   sq, bq);
+  if (e != cudaSuccess) return e;
+  const uint64_t ds[3] = {n, grows, 1};
+  const uint64_t ss[2] = {n * 4, grows * n * 4};
+  const uint32_t bs[3] = {32, G, 1};
+  return make_tmap_nd(&wm->scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, sc,
+                      3, ds, ss, bs);
 }
 
-template <int CH, bool SWIGLU>
-cudaError_t launch_acts(const float* x, const int32_t* qw, const float* sc, float* y, int M,
-                        int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  const int tiles = (slices_of<CH, SWIGLU>(N) + kWN - 1) / kWN;
-  return launch_split(gemv_acts_kernel<CH, SWIGLU>, ActsGeo<CH>::kAlloc, acts_cache<CH, SWIGLU>,
-                      tiles, x, qw, sc, y, M, N, K, di, s);
+// Activation descriptor: [M, K] row-major, box (32 CG inputs x kRows rows).
+template <typename L, typename XT>
+cudaError_t act_map(CUtensorMap* m, const XT* x, int M, int K) {
+  const uint64_t d[2] = {(uint64_t)K, (uint64_t)M};
+  const uint64_t s[1] = {(uint64_t)K * sizeof(XT)};
+  const uint32_t b[2] = {(uint32_t)(32 * L::kCG), (uint32_t)L::MI::kRows};
+  return make_tmap_nd(m,
+                      sizeof(XT) == 4 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                      : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                      CU_TENSOR_MAP_SWIZZLE_NONE, x, 2, d, s, b);
 }
 
-// Whether 4 tiles per warp (128 columns) fill the GPU at least about as well as 2: each width's
-// tiles with the split-K factor its resident clusters allow (plan_split). Wide tiles halve the
-// CTAs but share each activation fragment between more columns, so they win ties.
-template <typename KernW, typename KernN>
-cudaError_t prefer_wide(KernW kw, int smem_w, LaunchCache& cw, int tiles_w, KernN kn, int smem_n,
-                        LaunchCache& cn, int tiles_n, int K, const DeviceInfo& di, bool* wide) {
-  const LaunchData *lw = nullptr, *ln = nullptr;
-  cudaError_t e = launch_data(kw, smem_w, cw, di, &lw);
-  if (e != cudaSuccess) return e;
-  e = launch_data(kn, smem_n, cn, di, &ln);
-  if (e != cudaSuccess) return e;
+template <typename L, bool SWIGLU, typename XT, typename YT>
+struct Instance {
+  static LaunchCache cache;
+  static constexpr auto kernel = ws_gemv_kernel<L, SWIGLU, XT, YT>;
+
+  static cudaError_t data(const DeviceInfo& di, const LaunchData** ld) {
+    return launch_data(kernel, L::kAlloc, L::kThreads, cache, di, ld);
+  }
+  // Predicted fill of the GPU for this problem (see plan_split).
+  static cudaError_t fill(int M, int N, int K, const DeviceInfo& di, double* eff) {
+    const LaunchData* ld = nullptr;
+    cudaError_t e = data(di, &ld);
+    if (e != cudaSuccess) return e;
+    const int nz = (M + L::MI::kRows - 1) / L::MI::kRows;
+    const int stages = (K / kGroup + L::kG - 1) / L::kG;
+    (void)plan_split(*ld, (long long)cta_tiles<L, SWIGLU>(N) * nz, stages, di, eff);
+    return cudaSuccess;
+  }
+  static cudaError_t launch(const XT* x, const int32_t* qw, const float* sc, YT* y, int M, int N,
+                            int K, const DeviceInfo& di, cudaStream_t s) {
+    const LaunchData* ld = nullptr;
+    cudaError_t e = data(di, &ld);
+    if (e != cudaSuccess) return e;
+    const int nz = (M + L::MI::kRows - 1) / L::MI::kRows;
+    const int tiles = cta_tiles<L, SWIGLU>(N);
+    const int stages = (K / kGroup + L::kG - 1) / L::kG;
+    const int CK = plan_split(*ld, (long long)tiles * nz, stages, di, nullptr);
+    WeightMaps wm;
+    e = weight_maps<L, SWIGLU>(&wm, qw, sc, N, K);
+    if (e != cudaSuccess) return e;
+    CUtensorMap xm;
+    e = act_map<L, XT>(&xm, x, M, K);
+    if (e != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(tiles, CK, nz);
+    cfg.blockDim = dim3(L::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = CK;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = W4A16_PDL ? 2 : 1;
+    return cudaLaunchKernelEx(&cfg, kernel, wm, xm, y, M, N, K, device_error_word());
+  }
+};
+template <typename L, bool SWIGLU, typename XT, typename YT>
+LaunchCache Instance<L, SWIGLU, XT, YT>::cache;
+
+// Of two geometries (wide: more columns per CTA, narrow: fewer), launches the wide one unless the
+// narrow one fills the GPU more than 3 % better. Wide CTAs share each activation fragment
+// between more columns.
+template <typename Wide, typename Narrow, typename XT, typename YT>
+cudaError_t launch_best(const XT* x, const int32_t* qw, const float* sc, YT* y, int M, int N,
+                        int K, const DeviceInfo& di, cudaStream_t s) {
   double ew = 0.0, en = 0.0;
-  (void)plan_split(*lw, tiles_w, K / kGroup, di, &ew);
-  (void)plan_split(*ln, tiles_n, K / kGroup, di, &en);
-  *wide = ew * 1.03 >= en;
-  return cudaSuccess;
+  cudaError_t e = Wide::fill(M, N, K, di, &ew);
+  if (e != cudaSuccess) return e;
+  e = Narrow::fill(M, N, K, di, &en);
+  if (e != cudaSuccess) return e;
+  return ew * 1.03 >= en ? Wide::launch(x, qw, sc, y, M, N, K, di, s)
+                         : Narrow::launch(x, qw, sc, y, M, N, K, di, s);
 }
 
-// Up to 4 rows: 4 or 2 tiles per warp (prefer_wide); 5..8 rows: 2; 9 rows and more: the
-// activations-as-A kernel, 2 tiles, one 16-row slice per grid z (all slices in one launch, so CTAs
-// of several slices stream the same weight tiles at about the same time and share them through
-// L2).
+// The narrow form (8 tiles per CTA) of a wide geometry with W warps of CH tiles: the same warps
+// with half the tiles each, or half the warps when a fused SwiGLU warp needs its gate/up pair.
+constexpr int narrow_w(int W, int CH, bool swiglu) { return CH >= (swiglu ? 4 : 2) ? W : W / 2; }
+constexpr int narrow_ch(int W, int CH, bool swiglu) {
+  return CH >= (swiglu ? 4 : 2) ? CH / 2 : CH;
+}
+
 template <bool SWIGLU>
 cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* y, int M, int N,
                      int K, const DeviceInfo& di, cudaStream_t s) {
   if (M <= 4) {
-    constexpr int W = W4A16_WIDE_CH;
-    bool wide = true;
-    const cudaError_t e = prefer_wide(
-        gemv_codes_kernel<1, W, SWIGLU>, CodesGeo<1, W>::kAlloc, codes_cache<1, W, SWIGLU>,
-        (slices_of<W, SWIGLU>(N) + kWN - 1) / kWN, gemv_codes_kernel<1, 2, SWIGLU>,
-        CodesGeo<1, 2>::kAlloc, codes_cache<1, 2, SWIGLU>,
-        (slices_of<2, SWIGLU>(N) + kWN - 1) / kWN, K, di, &wide);
-    if (e != cudaSuccess) return e;
-    return wide ? launch_codes<1, W, SWIGLU>(x, qw, sc, y, M, N, K, di, s)
-                : launch_codes<1, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
+    using Wide = GeoN2<kN2W, kN2CH>;
+    using Narrow = GeoN2<narrow_w(kN2W, kN2CH, SWIGLU), narrow_ch(kN2W, kN2CH, SWIGLU)>;
+    return launch_best<Instance<Wide, SWIGLU, float, float>, Instance<Narrow, SWIGLU, float, float>>(
+        x, qw, sc, y, M, N, K, di, s);
   }
-  if (M <= 8) return launch_codes<2, 2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);
-  return launch_acts<2, SWIGLU>(x, qw, sc, y, M, N, K, di, s);  // 9+ rows, 16 per grid z
-}
-
-template <int NB, int CH>
-cudaError_t launch_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y, int M,
-                       int N, int K, const DeviceInfo& di, cudaStream_t s) {
-  const int tiles = (slices_of<CH, false>(N) + kWN - 1) / kWN;
-  return launch_split(gemv_b16_kernel<NB, CH>, CodesGeo<NB, CH>::kAlloc, b16_cache<NB, CH>, tiles,
-                      x, qw, sc, y, M, N, K, di, s);
+  if (M <= 8) {
+    using Wide = GeoK2a<kK2aW, kK2aCH>;
+    using Narrow = GeoK2a<narrow_w(kK2aW, kK2aCH, SWIGLU), narrow_ch(kK2aW, kK2aCH, SWIGLU)>;
+    return launch_best<Instance<Wide, SWIGLU, float, float>, Instance<Narrow, SWIGLU, float, float>>(
+        x, qw, sc, y, M, N, K, di, s);
+  }
+  using Wide = GeoK2b<kK2bW, kK2bCH>;
+  using Narrow = GeoK2b<narrow_w(kK2bW, kK2bCH, SWIGLU), narrow_ch(kK2bW, kK2bCH, SWIGLU)>;
+  return launch_best<Instance<Wide, SWIGLU, float, float>, Instance<Narrow, SWIGLU, float, float>>(
+      x, qw, sc, y, M, N, K, di, s);
 }
 
 }  // namespace
-
-cudaError_t launch_gemv_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
-                            int M, int N, int K, cudaStream_t s) {
-  DeviceInfo di;
-  cudaError_t e = device_info(&di);
-  if (e != cudaSuccess) return e;
-  if (M <= 8) {
-    constexpr int W = W4A16_B16_WIDE_CH;
-    bool wide = true;
-    e = prefer_wide(gemv_b16_kernel<1, W>, CodesGeo<1, W>::kAlloc, b16_cache<1, W>,
-                    (slices_of<W, false>(N) + kWN - 1) / kWN, gemv_b16_kernel<1, 2>,
-                    CodesGeo<1, 2>::kAlloc, b16_cache<1, 2>,
-                    (slices_of<2, false>(N) + kWN - 1) / kWN, K, di, &wide);
-    if (e != cudaSuccess) return e;
-    return wide ? launch_b16<1, W>(x, qw, sc, y, M, N, K, di, s)
-                : launch_b16<1, 2>(x, qw, sc, y, M, N, K, di, s);
-  }
-  if (M <= 16) return launch_b16<2, 2>(x, qw, sc, y, M, N, K, di, s);
-  return cudaErrorInvalidValue;
-}
 
 cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                         int N, int K, bool swiglu, cudaStream_t s) {
@@ -446,6 +450,23 @@ cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, floa
   if (e != cudaSuccess) return e;
   return swiglu ? dispatch<true>(x, qw, sc, y, M, N, K, di, s)
                 : dispatch<false>(x, qw, sc, y, M, N, K, di, s);
+}
+
+cudaError_t launch_gemv_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,
+                            int M, int N, int K, cudaStream_t s) {
+  DeviceInfo di;
+  cudaError_t e = device_info(&di);
+  if (e != cudaSuccess) return e;
+  constexpr int nw = narrow_w(kB16W, kB16CH, false), nch = narrow_ch(kB16W, kB16CH, false);
+  if (M <= 8)
+    return launch_best<Instance<GeoB16<1, kB16W, kB16CH>, false, uint16_t, uint16_t>,
+                       Instance<GeoB16<1, nw, nch>, false, uint16_t, uint16_t>>(x, qw, sc, y, M,
+                                                                                N, K, di, s);
+  if (M <= 16)
+    return launch_best<Instance<GeoB16<2, kB16W, kB16CH>, false, uint16_t, uint16_t>,
+                       Instance<GeoB16<2, nw, nch>, false, uint16_t, uint16_t>>(x, qw, sc, y, M,
+                                                                                N, K, di, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace w4a16

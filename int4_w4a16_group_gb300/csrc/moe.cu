@@ -18,19 +18,10 @@
 #include <stdint.h>
 
 #include "internal.h"
-#include "mma_core.cuh"
+#include "stream.cuh"
 
 namespace w4a16 {
 namespace {
-
-using namespace mma;
-
-constexpr int kWN = 8;           // warps (64-column slices) per CTA
-constexpr int kCH = 2;           // 16-byte chunks per lane per group
-constexpr int kRowsPerPass = 8;  // rows of one expert per pass over a weight tile
-
-template <int NB>
-using MoeGeo = Geo<NB, kCH, kWN, 4, 24576>;
 
 size_t align256(size_t v) { return (v + 255) & ~(size_t)255; }
 
@@ -119,63 +110,300 @@ __global__ void __launch_bounds__(1024) moe_route_kernel(const int32_t* __restri
 }
 
 // ---------------------------------------------------------------------------------- grouped GEMV
+//
+// Persistent warp-specialized CTAs (stream.cuh roles) walk jobs (active expert, 512-column
+// tile [gate/up: 256 gate + the matching 256 up columns], pass of up to 4 of the expert's rows):
+// each job streams its tile of the expert's packed weights once (TMA boxes with the expert as
+// the outermost coordinate) and accumulates the pass's rows in the two-term-column mode. The
+// prep warp gathers the pass's rows (one-row TMA boxes; rows past the pass read as zero). The
+// ring, chunk and barrier phases run on across jobs, so a CTA's next job streams while its last
+// one stores.
+
+using MoeL = ws::WsGeo<ws::kN2, 1, 4, 4, 2, 4, 8, 4>;
+constexpr int kPassRows = 4;
 
 struct GroupedArgs {
-  const float* src;          // gate/up: x [T, K]; down: h [P, I]
   const int* sorted_pair;    // expert-sorted pair indices
   int topk;
-  bool gather;               // gate/up: row = token of the pair; down: row = sorted position
+  bool gather;               // gate/up: source row = token of the pair; down: the sorted position
+  int src_rows;              // rows of the source (gate/up: T; down: P)
   const int* hdr;
   const int* off;
   const int* active;
   int N;                     // columns per expert (gate/up: 2I)
   int Kr;                    // reduction length (gate/up: K; down: I)
-  int tiles;
+  int tiles;                 // 512-column tiles per expert
   float* dst;                // gate/up: h [P, I]; down: y_pair [P, K]
   int ldd;
   unsigned int* err;
 };
 
-template <int NB, bool SWIGLU>
-__device__ __forceinline__ void grouped_pass(const GroupedArgs& a, const CUtensorMap* tq,
-                                             const CUtensorMap* ts, int e, int tile, int row0,
-                                             int rows, char* smem, int& seq) {
-  const int warp = threadIdx.x >> 5;
-  auto rowptr = [&](int m) {
-    const int p = row0 + m;
-    const int r = a.gather ? (a.sorted_pair[p] / a.topk) : p;
-    return a.src + (size_t)r * a.Kr;
-  };
-  float acc[kCH][2][NB][4];
-  stream_groups<NB, kCH, SWIGLU, kWN, MoeGeo<NB>>(rowptr, rows, tq, ts, e, a.N, 0,
-                                                   a.Kr / kGroup, tile * kWN, smem, seq, a.err,
-                                                   acc);
-  store_direct<NB, kCH, SWIGLU>(acc, tile * kWN + warp, a.N, rows, a.dst + (size_t)row0 * a.ldd);
+// Job cursor: (active expert index, tile, pass) in the order every role of a CTA walks them.
+struct JobCursor {
+  long long item;  // active expert index * tiles + tile
+  int pass;
+  __device__ __forceinline__ JobCursor(long long start) : item(start), pass(0) {}
+  // Fills the job; returns false past the end.
+  __device__ __forceinline__ bool get(const GroupedArgs& a, int n_active, int* e, int* tile,
+                                      int* r0, int* rows) const {
+    if (item >= (long long)n_active * a.tiles) return false;
+    const int ai = (int)(item / a.tiles);
+    *tile = (int)(item - (long long)ai * a.tiles);
+    *e = a.active[ai];
+    const int o0 = a.off[*e], o1 = a.off[*e + 1];
+    *r0 = o0 + kPassRows * pass;
+    *rows = min(kPassRows, o1 - *r0);
+    return true;
+  }
+  __device__ __forceinline__ void next(const GroupedArgs& a, int rows_total) {
+    if (kPassRows * (pass + 1) < rows_total) {
+      ++pass;
+    } else {
+      pass = 0;
+      item += gridDim.x;
+    }
+  }
+};
+
+__device__ __forceinline__ int expert_rows(const GroupedArgs& a, int e) {
+  return a.off[e + 1] - a.off[e];
 }
 
 template <bool SWIGLU>
-__global__ void __launch_bounds__(kWN * 32, 2)
-    moe_grouped_kernel(const __grid_constant__ CUtensorMap tq,
-                       const __grid_constant__ CUtensorMap ts, GroupedArgs a) {
-  extern __shared__ __align__(1024) char smem_raw[];
-  char* smem = align1024(smem_raw);
-  init_barriers<MoeGeo<2>>(smem, kWN);
-  int seq = 0;
-  const int n_active = a.hdr[0];
-  const long long total = (long long)n_active * a.tiles;
-  for (long long item = blockIdx.x; item < total; item += gridDim.x) {
-    const int ai = (int)(item / a.tiles);
-    const int tile = (int)(item - (long long)ai * a.tiles);
-    const int e = a.active[ai];
-    const int r0 = a.off[e];
-    const int rows = a.off[e + 1] - r0;
-    for (int c0 = 0; c0 < rows; c0 += kRowsPerPass) {
-      const int mr = (rows - c0) < kRowsPerPass ? (rows - c0) : kRowsPerPass;
-      if (mr <= 4)
-        grouped_pass<1, SWIGLU>(a, &tq, &ts, e, tile, r0 + c0, mr, smem, seq);
-      else
-        grouped_pass<2, SWIGLU>(a, &tq, &ts, e, tile, r0 + c0, mr, smem, seq);
+__device__ __forceinline__ void moe_producer(const ws::WeightMaps& wm, char* base,
+                                             const GroupedArgs& a, int n_active) {
+  using L = MoeL;
+  constexpr int R = L::kR, G = L::kG;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kAbortOff);
+  const ws::Bars<L> bars(base);
+  const uint32_t codes = ws::smem_u32(base + L::kCodeOff);
+  const uint32_t scales = ws::smem_u32(base + L::kScaleOff);
+  const int nst = (a.Kr / kGroup + G - 1) / G;
+  int st = 0;
+  uint32_t ph = 0;
+  long long issued = 0;
+  bool ok = true;
+  JobCursor jc(blockIdx.x);
+  int e, tile, r0, rows;
+  while (ok && jc.get(a, n_active, &e, &tile, &r0, &rows)) {
+    for (int s = 0; s < nst; ++s) {
+      if (issued >= R && !ws::wait_phase(bars.empty + 8 * st, ph ^ 1, abort_flag)) {
+        ws::raise_abort(abort_flag, a.err);
+        ok = false;
+        break;
+      }
+      ws::issue_stage<L::kW, L::kCH, G, SWIGLU, L>(wm, codes + st * L::kCodeStage,
+                                                    scales + st * L::kScaleStage,
+                                                    bars.full + 8 * st, s * G, tile, a.N, e);
+      ++issued;
+      if (++st == R) {
+        st = 0;
+        ph ^= 1;
+      }
     }
+    jc.next(a, expert_rows(a, e));
+  }
+  for (long long s = issued > R ? issued - R : 0; s < issued; ++s)
+    (void)mma::mbar_wait(bars.full + 8 * (int)(s % R), (uint32_t)((s / R) & 1),
+                         ws::kWaitLimitNs / 16);
+}
+
+// Issues the raw rows of one chunk (lane 0): row m < rows is source row src(r0 + m), the others
+// are read past the end of the source (zeros).
+__device__ __forceinline__ void moe_issue_chunk(const CUtensorMap* xmap, const GroupedArgs& a,
+                                                uint32_t dst, uint32_t bar, int k0, int r0,
+                                                int rows) {
+  using L = MoeL;
+  ws::mbar_expect_tx(bar, L::kXRawBytes);
+  for (int m = 0; m < kPassRows; ++m) {
+    int src = a.src_rows;
+    if (m < rows) src = a.gather ? a.sorted_pair[r0 + m] / a.topk : r0 + m;
+    ws::tma_load_2d(dst + m * (L::kXRawBytes / kPassRows), xmap, k0, src, bar);
+  }
+}
+
+__device__ __forceinline__ void moe_prep(const CUtensorMap* xmap, char* base, const GroupedArgs& a,
+                                         int n_active) {
+  using L = MoeL;
+  constexpr int CG = L::kCG;
+  const int lane = threadIdx.x & 31;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kAbortOff);
+  const ws::Bars<L> bars(base);
+  const uint32_t xraw = ws::smem_u32(base + L::kXRawOff);
+  const int Gt = a.Kr / kGroup;
+  const int nch = (Gt + CG - 1) / CG;  // chunks per job
+  // Issue cursor (lane 0): job and chunk of the next raw chunk to load.
+  JobCursor ic(blockIdx.x);
+  int ic_chunk = 0;
+  long long issued = 0;
+  auto issue_next = [&](int buf) {  // lane 0; returns nothing, advances the cursor
+    int e, tile, r0, rows;
+    if (!ic.get(a, n_active, &e, &tile, &r0, &rows)) return;
+    moe_issue_chunk(xmap, a, xraw + buf * L::kXRawBytes, bars.xfull + 8 * buf,
+                    32 * CG * ic_chunk, r0, rows);
+    ++issued;
+    if (++ic_chunk == nch) {
+      ic_chunk = 0;
+      ic.next(a, expert_rows(a, e));
+    }
+  };
+  if (lane == 0) {
+    issue_next(0);
+    issue_next(1);
+  }
+  long long c = 0;  // chunks converted so far
+  bool ok = true;
+  JobCursor jc(blockIdx.x);
+  int e, tile, r0, rows;
+  while (ok && jc.get(a, n_active, &e, &tile, &r0, &rows)) {
+    for (int cj = 0; cj < nch; ++cj, ++c) {
+      const int b = (int)(c & 1);
+      const uint32_t par = (uint32_t)((c >> 1) & 1);
+      bool good = ws::wait_phase(bars.xfull + 8 * b, par, abort_flag);
+      if (good && c >= 2) good = ws::wait_phase(bars.fempty + 8 * b, par ^ 1, abort_flag);
+      if (!__all_sync(0xffffffffu, good)) {
+        if (lane == 0) ws::raise_abort(abort_flag, a.err);
+        ok = false;
+        break;
+      }
+      const int ngr = Gt - cj * CG < CG ? Gt - cj * CG : CG;
+      ws::prep_chunk<ws::kN2, 1, float, L>(base, b, ngr);
+      ws::mbar_arrive(bars.ffull + 8 * b);
+      ws::fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) issue_next(b);
+    }
+    jc.next(a, expert_rows(a, e));
+  }
+  if (lane == 0) {
+    for (long long i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+      (void)mma::mbar_wait(bars.xfull + 8 * (int)(i & 1), (uint32_t)((i >> 1) & 1),
+                           ws::kWaitLimitNs / 16);
+  }
+}
+
+template <bool SWIGLU>
+__device__ __forceinline__ void moe_consumers(char* base, const GroupedArgs& a, int n_active) {
+  using L = MoeL;
+  constexpr int CH = L::kCH, G = L::kG, R = L::kR, CG = L::kCG, W = L::kW;
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3, w = (threadIdx.x >> 5) - 2;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(base + L::kAbortOff);
+  const ws::Bars<L> bars(base);
+  const int h = mma::lane_chunk(g);
+  const uint32_t codes = ws::smem_u32(base + L::kCodeOff);
+  const uint32_t scales = ws::smem_u32(base + L::kScaleOff) + h * 16;
+  const uint32_t frag = ws::smem_u32(base + L::kFragOff) + lane * 16;
+  const int* fexp = reinterpret_cast<const int*>(base + L::kExpOff);
+  const int Gt = a.Kr / kGroup;
+  const int nch = (Gt + CG - 1) / CG;
+  int st = 0;
+  uint32_t ph = 0;
+  long long c = 0;
+  bool ok = true;
+  JobCursor jc(blockIdx.x);
+  int e, tile, r0, rows;
+  while (ok && jc.get(a, n_active, &e, &tile, &r0, &rows)) {
+    ws::Acc<CH, 1> acc;
+#pragma unroll
+    for (int cc = 0; cc < CH; ++cc)
+#pragma unroll
+      for (int T = 0; T < 2; ++T)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) acc.v[cc][T][0][r] = 0.0f;
+    int ex = 0;
+    for (int cj = 0; cj < nch && ok; ++cj, ++c) {
+      const int b = (int)(c & 1);
+      ok = ws::wait_phase(bars.ffull + 8 * b, (uint32_t)((c >> 1) & 1), abort_flag);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      const int en = fexp[16 * b + t];
+      if (cj > 0) {
+        const int d = ex - en;
+        const float f = mma::exp2i(d >> 1) * mma::exp2i(d - (d >> 1));
+#pragma unroll
+        for (int cc = 0; cc < CH; ++cc)
+#pragma unroll
+          for (int T = 0; T < 2; ++T)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) acc.v[cc][T][0][r] *= f;
+      }
+      ex = en;
+      const int ngr = Gt - cj * CG < CG ? Gt - cj * CG : CG;
+      const uint32_t fr = frag + b * L::kFragBytes;
+      for (int q = 0; q < ngr; q += G) {
+        if (!ws::wait_phase(bars.full + 8 * st, ph, abort_flag)) ok = false;
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        const uint32_t cs = codes + st * L::kCodeStage, ss = scales + st * L::kScaleStage;
+#pragma unroll(ws::kGroupUnroll)
+        for (int j = 0; j < G; ++j)
+          if (q + j < ngr)
+            ws::consume_group<ws::kN2, 1, W, CH, SWIGLU, L>(cs + ws::code_offset(j, t, h),
+                                                            ss + j * 128,
+                                                            fr + (q + j) * 512, w, acc);
+        __syncwarp();
+        if (lane == 0) ws::mbar_arrive(bars.empty + 8 * st);
+        if (++st == R) {
+          st = 0;
+          ph ^= 1;
+        }
+      }
+      __syncwarp();
+      if (ok && lane == 0) ws::mbar_arrive(bars.fempty + 8 * b);
+    }
+    if (!ok) break;
+    // lane row t of the pass -> destination row r0 + t
+    if (t < rows) {
+      const float f = mma::exp2i(ex - 14);
+      float* dst = a.dst + (size_t)(r0 + t) * a.ldd;
+      const int h4 = 4 * h;
+      if constexpr (SWIGLU) {
+        constexpr int H = CH / 2, TT = L::kTiles / 2;
+#pragma unroll
+        for (int cc = 0; cc < H; ++cc) {
+          const int j = 32 * (tile * TT + w * H + cc) + h4;
+          const float4 gv = ws::lane_result<ws::kN2, CH, 1>(acc, cc, 0, 0, f);
+          const float4 uv = ws::lane_result<ws::kN2, CH, 1>(acc, cc + H, 0, 0, f);
+          if (j < (a.N >> 1))
+            *reinterpret_cast<float4*>(dst + j) =
+                make_float4(mma::silu_f(gv.x) * uv.x, mma::silu_f(gv.y) * uv.y,
+                            mma::silu_f(gv.z) * uv.z, mma::silu_f(gv.w) * uv.w);
+        }
+      } else {
+#pragma unroll
+        for (int cc = 0; cc < CH; ++cc) {
+          const int col = 32 * (tile * L::kTiles + w * CH + cc) + h4;
+          if (col < a.N)
+            *reinterpret_cast<float4*>(dst + col) =
+                ws::lane_result<ws::kN2, CH, 1>(acc, cc, 0, 0, f);
+        }
+      }
+    }
+    jc.next(a, expert_rows(a, e));
+  }
+  if (!ok && lane == 0) ws::raise_abort(abort_flag, a.err);
+}
+
+template <bool SWIGLU>
+__global__ void __launch_bounds__(MoeL::kThreads, 2)
+    moe_grouped_kernel(const __grid_constant__ ws::WeightMaps wm,
+                       const __grid_constant__ CUtensorMap xmap, GroupedArgs a) {
+  extern __shared__ __align__(1024) char smem_raw[];
+  char* base = mma::align1024(smem_raw);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_active = a.hdr[0];
+  ws::init_roles<MoeL>(base);
+  __syncthreads();
+  if (warp == 0) {
+    if (lane == 0) moe_producer<SWIGLU>(wm, base, a, n_active);
+  } else if (warp == 1) {
+    moe_prep(&xmap, base, a, n_active);
+  } else {
+    moe_consumers<SWIGLU>(base, a, n_active);
   }
 }
 
@@ -224,37 +452,61 @@ __global__ void topk_softmax_kernel(const float* __restrict__ logits, float* __r
   }
 }
 
-// Both NB paths of the grouped kernel share one shared-memory buffer (the larger layout); the
-// rings and barriers sit at the same offsets in both.
-static_assert(MoeGeo<1>::kBarOff == MoeGeo<2>::kBarOff, "shared barrier offset");
-constexpr int kMoeSmem =
-    MoeGeo<2>::kAlloc > MoeGeo<1>::kAlloc ? MoeGeo<2>::kAlloc : MoeGeo<1>::kAlloc;
-
 template <bool SWIGLU>
-cudaError_t launch_grouped(const GroupedArgs& a, const int32_t* qw, const float* sc, int E,
-                           const DeviceInfo& di, cudaStream_t s) {
+cudaError_t launch_grouped(const GroupedArgs& a, const float* src, const int32_t* qw,
+                           const float* sc, int E, const DeviceInfo& di, cudaStream_t s) {
+  using L = MoeL;
   static PerDeviceOnce<int> occ_cache;  // resident CTAs per SM
   auto kern = moe_grouped_kernel<SWIGLU>;
   const int* occ = nullptr;
   cudaError_t e = occ_cache.get(di.device, [&](int& o) {
-    cudaError_t r =
-        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kMoeSmem);
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         L::kAlloc);
     if (r != cudaSuccess) return r;
     int n = 0;
-    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kWN * 32, kMoeSmem);
+    r = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, L::kThreads, L::kAlloc);
     if (r != cudaSuccess) return r;
     o = n < 1 ? 1 : n;
     return cudaSuccess;
   }, &occ);
   if (e != cudaSuccess) return e;
-  CUtensorMap tq, ts;
-  e = make_tmap(&tq, 0, qw, (uint64_t)a.N, (uint64_t)(a.Kr / 8), (uint64_t)E, 32,
-                            kRows);
+  // Weights [E][Kr/8][N] / [E][Kr/32][N]: columns x rows x 32-column tiles [x gate/up half]
+  // x expert, boxes of one stage of a CTA's tiles.
+  ws::WeightMaps wm;
+  wm.fast = 1;
+  const uint64_t n = (uint64_t)a.N, rows = (uint64_t)a.Kr / 8, grows = (uint64_t)a.Kr / kGroup;
+  const uint64_t ne = (uint64_t)E;
+  if (SWIGLU) {
+    const uint64_t I = n / 2;
+    const uint64_t dq[5] = {32, rows, I / 32, 2, ne}, sq[4] = {n * 4, 128, I * 4, rows * n * 4};
+    const uint32_t bq[5] = {32, 4 * L::kG, L::kTiles / 2, 2, 1};
+    e = make_tmap_nd(&wm.codes, CU_TENSOR_MAP_DATA_TYPE_INT32, CU_TENSOR_MAP_SWIZZLE_128B, qw, 5,
+                     dq, sq, bq);
+    if (e != cudaSuccess) return e;
+    const uint64_t ds[5] = {32, grows, I / 32, 2, ne}, ss[4] = {n * 4, 128, I * 4, grows * n * 4};
+    const uint32_t bs[5] = {32, L::kG, L::kTiles / 2, 2, 1};
+    e = make_tmap_nd(&wm.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, sc,
+                     5, ds, ss, bs);
+  } else {
+    const uint64_t dq[4] = {32, rows, n / 32, ne}, sq[3] = {n * 4, 128, rows * n * 4};
+    const uint32_t bq[4] = {32, 4 * L::kG, L::kTiles, 1};
+    e = make_tmap_nd(&wm.codes, CU_TENSOR_MAP_DATA_TYPE_INT32, CU_TENSOR_MAP_SWIZZLE_128B, qw, 4,
+                     dq, sq, bq);
+    if (e != cudaSuccess) return e;
+    const uint64_t ds[4] = {32, grows, n / 32, ne}, ss[3] = {n * 4, 128, grows * n * 4};
+    const uint32_t bs[4] = {32, L::kG, L::kTiles, 1};
+    e = make_tmap_nd(&wm.scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, sc,
+                     4, ds, ss, bs);
+  }
   if (e != cudaSuccess) return e;
-  e = make_tmap(&ts, 1, sc, (uint64_t)a.N, (uint64_t)(a.Kr / kGroup), (uint64_t)E, 32,
-                kRows / 4);
+  // Source rows [src_rows][Kr], one row per box (the prep warp gathers a pass's rows).
+  CUtensorMap xm;
+  const uint64_t dx[2] = {(uint64_t)a.Kr, (uint64_t)a.src_rows}, sx[1] = {(uint64_t)a.Kr * 4};
+  const uint32_t bx[2] = {32 * L::kCG, 1};
+  e = make_tmap_nd(&xm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, CU_TENSOR_MAP_SWIZZLE_NONE, src, 2, dx,
+                   sx, bx);
   if (e != cudaSuccess) return e;
-  kern<<<di.sm_count * *occ, kWN * 32, kMoeSmem, s>>>(tq, ts, a);
+  kern<<<di.sm_count * *occ, L::kThreads, L::kAlloc, s>>>(wm, xm, a);
   return cudaGetLastError();
 }
 
@@ -308,30 +560,30 @@ cudaError_t launch_moe_block(const float* x, const int32_t* ids, const float* w,
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
   GroupedArgs gu;
-  gu.src = x;
   gu.sorted_pair = sorted;
   gu.topk = topk;
   gu.gather = true;
+  gu.src_rows = T;
   gu.hdr = hdr;
   gu.off = off;
   gu.active = active;
   gu.err = device_error_word();
   gu.N = 2 * I;
   gu.Kr = K;
-  gu.tiles = ((I + 16 * kCH - 1) / (16 * kCH) + kWN - 1) / kWN;
+  gu.tiles = (I + 16 * MoeL::kTiles - 1) / (16 * MoeL::kTiles);
   gu.dst = h;
   gu.ldd = I;
-  if ((e = launch_grouped<true>(gu, qw_gu, sc_gu, E, di, s)) != cudaSuccess) return e;
+  if ((e = launch_grouped<true>(gu, x, qw_gu, sc_gu, E, di, s)) != cudaSuccess) return e;
 
   GroupedArgs dn = gu;
-  dn.src = h;
   dn.gather = false;
+  dn.src_rows = P;
   dn.N = K;
   dn.Kr = I;
-  dn.tiles = ((K + 32 * kCH - 1) / (32 * kCH) + kWN - 1) / kWN;
+  dn.tiles = (K + 32 * MoeL::kTiles - 1) / (32 * MoeL::kTiles);
   dn.dst = ypair;
   dn.ldd = K;
-  if ((e = launch_grouped<false>(dn, qw_dn, sc_dn, E, di, s)) != cudaSuccess) return e;
+  if ((e = launch_grouped<false>(dn, h, qw_dn, sc_dn, E, di, s)) != cudaSuccess) return e;
 
   float* ys = nullptr;
   if (qs_gu) {

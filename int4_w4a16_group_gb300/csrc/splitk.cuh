@@ -30,10 +30,11 @@ __device__ __forceinline__ void cluster_finish(cg::cluster_group& cluster, float
   cluster.sync();
   if (SWIGLU) {
     const int I = N >> 1;
-    const int per = kOut / CK;
+    const int per = (kOut + CK - 1) / CK;  // any cluster size: the last ranks may get fewer
     for (int idx = threadIdx.x; idx < M * per; idx += blockDim.x) {
       const int m = idx / per;
       const int o = rank * per + (idx - m * per);
+      if (o >= kOut) continue;
       float gs = 0.0f, us = 0.0f;
       for (int q = 0; q < CK; ++q) {
         const float* r = cluster.map_shared_rank(red, q);
@@ -44,10 +45,11 @@ __device__ __forceinline__ void cluster_finish(cg::cluster_group& cluster, float
       if (out < I) store_out(y, (size_t)m * I + out, silu_f(gs) * us);
     }
   } else {
-    const int per = kCols / CK;
+    const int per = (kCols + CK - 1) / CK;
     for (int idx = threadIdx.x; idx < M * per; idx += blockDim.x) {
       const int m = idx / per;
       const int lc = rank * per + (idx - m * per);
+      if (lc >= kCols) continue;
       float s = 0.0f;
       for (int q = 0; q < CK; ++q) s += cluster.map_shared_rank(red, q)[m * kCols + lc];
       const int out = tile * kCols + lc;
