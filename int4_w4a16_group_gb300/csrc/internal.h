@@ -85,6 +85,7 @@ cudaError_t launch_dequantize(const int32_t* qw, const float* sc, int K, int N, 
 cudaError_t launch_gemv(const float* x, const int32_t* qw, const float* sc, float* y, int M,
                         int N, int K, bool swiglu, cudaStream_t s);
 constexpr int kGemvMaxM = 16;
+
 constexpr int kGemvMaxRowsPerLaunch = kGemvMaxM * 4096;
 // The same for bf16 activations and bf16 output (y[M, N] = bf16(x @ W)), M <= 16.
 cudaError_t launch_gemv_b16(const uint16_t* x, const int32_t* qw, const float* sc, uint16_t* y,

@@ -252,6 +252,7 @@ __device__ __forceinline__ void moe_prep(const CUtensorMap* xmap, char* base, co
     issue_next(1);
   }
   long long c = 0;  // chunks converted so far
+  int eprev[1] = {0};
   bool ok = true;
   JobCursor jc(blockIdx.x);
   int e, tile, r0, rows;
@@ -267,7 +268,7 @@ __device__ __forceinline__ void moe_prep(const CUtensorMap* xmap, char* base, co
         break;
       }
       const int ngr = Gt - cj * CG < CG ? Gt - cj * CG : CG;
-      ws::prep_chunk<ws::kN2, 1, float, L>(base, b, ngr);
+      ws::prep_chunk<ws::kN2, 1, float, L>(base, b, ngr, eprev, cj == 0);
       ws::mbar_arrive(bars.ffull + 8 * b);
       ws::fence_proxy_async_smem();
       __syncwarp();
@@ -318,8 +319,9 @@ __device__ __forceinline__ void moe_consumers(char* base, const GroupedArgs& a, 
         ok = false;
         break;
       }
-      const int en = fexp[16 * b + t];
-      if (cj > 0) {
+      const bool changed = cj == 0 || fexp[32 * b + 16] != 0;
+      const int en = changed ? fexp[32 * b + t] : ex;
+      if (cj > 0 && changed) {
         const int d = ex - en;
         const float f = mma::exp2i(d >> 1) * mma::exp2i(d - (d >> 1));
 #pragma unroll

@@ -153,7 +153,7 @@ struct ModeInfo {
 //   scales R stages x kTiles x (G x 128 B)
 //   xraw   2 x (kRows x 32 CG activations)         -- raw activation chunks (TMA)
 //   frag   2 x (CG x kFragGroup)                   -- prepared B fragments
-//   fexp   2 x 16 ints                             -- each row's exponent per chunk buffer
+//   fexp   2 x 32 ints                             -- row exponents (16) and a changed flag
 //   bars   full[R], empty[R], xfull[2], ffull[2], fempty[2]; abort flag
 // CG = groups per activation chunk (at most 8: a TMA box row holds at most 256 elements).
 template <int MODE, int NB, int W, int CH, int G, int R, int CG, int XBYTES>
@@ -181,7 +181,7 @@ struct WsGeo {
   static constexpr int kXRawOff = kScaleOff + R * kScaleStage;
   static constexpr int kFragOff = kXRawOff + 2 * kXRawBytes;
   static constexpr int kExpOff = kFragOff + 2 * kFragBytes;
-  static constexpr int kBarOff = kExpOff + 2 * 16 * 4;
+  static constexpr int kBarOff = kExpOff + 2 * 32 * 4;
   static constexpr int kNumBars = 2 * R + 6;
   static constexpr int kAbortOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kAbortOff + 16;
@@ -195,10 +195,11 @@ struct WsGeo {
 // ------------------------------------------------------------------------------ prep warp
 
 // Exponent of a row's largest magnitude (|x| < 2^(e+1)), clamped so that 2^(14 - e) and the
-// result factors stay normal floats.
+// result factors stay normal floats; kNoExp for an all-zero row.
+constexpr int kNoExp = -1000;
 __device__ __forceinline__ int row_exponent(float amax) {
-  int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-  if (amax == 0.0f) ex = 0;
+  if (amax == 0.0f) return kNoExp;
+  const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
   return ex < -100 ? -100 : (ex > 100 ? 100 : ex);
 }
 
@@ -234,14 +235,20 @@ __device__ __forceinline__ uint4 frag_of(const float (&o)[8]) {
 
 // Converts raw chunk `buf` (ngr groups) into B fragments and row exponents. Lane (g, t) of the
 // prep warp writes exactly the 16-byte pieces consumer lane (g, t) will read.
+// Row exponents are sticky: a row keeps the exponent of earlier chunks (eprev) unless this
+// chunk's largest magnitude would not fit under it (fp16 holds up to 2^16 times 2^(e - 14), so
+// a chunk exponent up to e + 1 fits); the chunk's flag word tells the consumers whether any
+// row's exponent changed (only then do they rescale their accumulators). `first` starts a new
+// sequence of chunks.
 template <int MODE, int NB, typename XT, typename L>
-__device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr) {
+__device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr,
+                                           int (&eprev)[MODE == kN2 ? 1 : NB], bool first) {
   using MI = typename L::MI;
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   constexpr int kRowBytes = L::kCG * 32 * (int)sizeof(XT);
   const uint32_t raw = smem_u32(base + L::kXRawOff + buf * L::kXRawBytes);
   char* frag = base + L::kFragOff + buf * L::kFragBytes;
-  int* fexp = reinterpret_cast<int*>(base + L::kExpOff) + buf * 16;
+  int* fexp = reinterpret_cast<int*>(base + L::kExpOff) + buf * 32;
   constexpr int kLaneRows = MODE == kN2 ? 1 : NB;  // rows this lane converts
   int rows[kLaneRows];
 #pragma unroll
@@ -261,9 +268,20 @@ __device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr) {
     }
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-    ex[i] = row_exponent(amax);
-    if (t == 0 && (MODE != kN2 || (g & 1) == 0)) fexp[rows[i]] = ex[i];
+    const int ec = row_exponent(amax);
+    // a row with no nonzero value so far takes the chunk's exponent
+    ex[i] = (first || eprev[i] == kNoExp || ec > eprev[i] + 1) ? ec : eprev[i];
+    if (t == 0 && (MODE != kN2 || (g & 1) == 0)) fexp[rows[i]] = ex[i] == kNoExp ? 0 : ex[i];
   }
+  bool changed = false;
+#pragma unroll
+  for (int i = 0; i < kLaneRows; ++i) {
+    changed |= !first && ex[i] != eprev[i];
+    eprev[i] = ex[i];
+    if (ex[i] == kNoExp) ex[i] = 0;  // zero rows: any scale
+  }
+  changed = __any_sync(0xffffffffu, changed);
+  if (lane == 0) fexp[16] = changed ? 1 : 0;
 
   for (int j = 0; j < ngr; ++j) {
 #pragma unroll
@@ -491,6 +509,7 @@ __device__ __forceinline__ void prep_loop(const CUtensorMap* xmap, char* base, i
   const Bars<L> bars(base);
   const uint32_t xraw = smem_u32(base + L::kXRawOff);
   const int nch = (nq + CG - 1) / CG;
+  int eprev[L::kMode == kN2 ? 1 : L::kNB] = {};
   int issued = nch < 2 ? nch : 2;
   if (lane == 0) {
     dependency_wait();  // the activations may be the previous kernel's output
@@ -509,7 +528,7 @@ __device__ __forceinline__ void prep_loop(const CUtensorMap* xmap, char* base, i
       break;
     }
     const int ngr = nq - c * CG < CG ? nq - c * CG : CG;
-    prep_chunk<L::kMode, L::kNB, XT, L>(base, b, ngr);
+    prep_chunk<L::kMode, L::kNB, XT, L>(base, b, ngr, eprev, c == 0);
     mbar_arrive(bars.ffull + 8 * b);
     fence_proxy_async_smem();  // this lane's reads of the raw chunk precede its next TMA refill
     __syncwarp();
@@ -592,9 +611,10 @@ __device__ __forceinline__ bool consumer_loop(char* base, int nq, int w, unsigne
       break;
     }
     int en[LR::kN];
+    const bool changed = c == 0 || fexp[32 * b + 16] != 0;  // same for the whole warp
 #pragma unroll
-    for (int i = 0; i < LR::kN; ++i) en[i] = fexp[16 * b + LR::row(t, i)];
-    if (c > 0) {
+    for (int i = 0; i < LR::kN; ++i) en[i] = changed ? fexp[32 * b + LR::row(t, i)] : ex[i];
+    if (c > 0 && changed) {
       // accumulators from chunk units 2^(ex - 14) to 2^(en - 14)
 #pragma unroll
       for (int i = 0; i < LR::kN; ++i) {

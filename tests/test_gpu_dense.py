@@ -83,6 +83,28 @@ def test_gemm_handmade_extremes(w4):
     assert_close_rows(host(y), oracle.gemm(x, qw, sc), FP32_TOL, "extremes")
 
 
+@pytest.mark.parametrize("M", [3, 8, 16, 20])
+def test_gemm_activation_range_along_k(w4, M):
+    """Activations whose magnitude jumps by 1e4 up or down along K (and a row that is zero in
+    its first half): the kernels' per-row exponents must follow (raised when larger values
+    arrive, kept when smaller ones do) without losing the float32 accuracy."""
+    K, N = 2048, 520
+    W = synth.weights(K, N, seed=31 + M, outliers=True)
+    x = synth.activations(M, K, seed=32 + M)
+    x[: M // 2, : K // 2] *= 1e-4
+    x[M // 2:, K // 2:] *= 1e-4
+    x[-1, : K // 2] = 0.0
+    qo, so = oracle.quantize_w4a16(W)
+    for swiglu in (False, True):
+        if swiglu:
+            y = w4.w4a16_gemm_swiglu(dev(x), dev(qo), dev(so))
+            ref = oracle.swiglu_gemm(x, qo, so)
+        else:
+            y = w4.w4a16_gemm(dev(x), dev(qo), dev(so))
+            ref = oracle.gemm(x, qo, so)
+        assert_close_rows(host(y), ref, FP32_TOL, f"range along K, M={M}, swiglu={swiglu}")
+
+
 def test_gemm_zero_weights_and_empty(w4):
     K, N = 256, 128
     qw, sc = oracle.quantize_w4a16(np.zeros((K, N), dtype=np.float32))
