@@ -47,7 +47,10 @@ using ws::WeightMaps;
 #define W4A16_K2A_W 4
 #endif
 #ifndef W4A16_K2A_R
-#define W4A16_K2A_R 4
+#define W4A16_K2A_R 3
+#endif
+#ifndef W4A16_K2A_CG
+#define W4A16_K2A_CG 8
 #endif
 #ifndef W4A16_K2B_W
 #define W4A16_K2B_W 4
@@ -64,6 +67,12 @@ using ws::WeightMaps;
 #ifndef W4A16_B16_R
 #define W4A16_B16_R 4
 #endif
+#ifndef W4A16_B16B_R
+#define W4A16_B16B_R 3
+#endif
+#ifndef W4A16_B16B_CG
+#define W4A16_B16B_CG 8
+#endif
 #ifndef W4A16_MINB
 #define W4A16_MINB 2
 #endif
@@ -77,11 +86,13 @@ using ws::WeightMaps;
 template <int W, int CH>
 using GeoN2 = ws::WsGeo<ws::kN2, 1, W, CH, 2, W4A16_N2_R * 16 / (W * CH), 8, 4>;
 template <int W, int CH>
-using GeoK2a = ws::WsGeo<ws::kK2, 1, W, CH, 2, W4A16_K2A_R * 16 / (W * CH), 8, 4>;
+using GeoK2a = ws::WsGeo<ws::kK2, 1, W, CH, 2, W4A16_K2A_R * 16 / (W * CH), W4A16_K2A_CG, 4>;
 template <int W, int CH>
 using GeoK2b = ws::WsGeo<ws::kK2, 2, W, CH, 2, W4A16_K2B_R * 16 / (W * CH), W4A16_K2B_CG, 4>;
 template <int NB, int W, int CH>
-using GeoB16 = ws::WsGeo<ws::kK1, NB, W, CH, 2, W4A16_B16_R * 16 / (W * CH), 8, 2>;
+using GeoB16 = ws::WsGeo<ws::kK1, NB, W, CH, 2,
+                         (NB == 1 ? W4A16_B16_R : W4A16_B16B_R) * 16 / (W * CH),
+                         NB == 1 ? 8 : W4A16_B16B_CG, 2>;
 constexpr int kN2W = W4A16_N2_W, kN2CH = 16 / W4A16_N2_W;
 constexpr int kK2aW = W4A16_K2A_W, kK2aCH = 16 / W4A16_K2A_W;
 constexpr int kK2bW = W4A16_K2B_W, kK2bCH = 16 / W4A16_K2B_W;

@@ -127,6 +127,27 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity,
   return true;
 }
 
+// As wait_phase, but polls: try_wait without a sleep hint (the hardware's own short suspend), for
+// the consumer warps, whose wake-up latency is on the critical path.
+__device__ __forceinline__ bool wait_phase_poll(uint32_t bar, uint32_t parity,
+                                                const volatile int* abort_flag) {
+  if (mma::mbar_try_wait_poll(bar, parity)) return true;
+  const uint64_t t0 = mma::global_ns();
+  uint32_t n = 0;
+  while (!mma::mbar_try_wait_poll(bar, parity)) {
+    if ((++n & 255u) == 0 && (*abort_flag || mma::global_ns() - t0 > kWaitLimitNs)) return false;
+  }
+  return true;
+}
+#ifndef W4A16_POLL_CONSUMER
+#define W4A16_POLL_CONSUMER 0
+#endif
+__device__ __forceinline__ bool wait_consumer(uint32_t bar, uint32_t parity,
+                                              const volatile int* abort_flag) {
+  return W4A16_POLL_CONSUMER ? wait_phase_poll(bar, parity, abort_flag)
+                             : wait_phase(bar, parity, abort_flag);
+}
+
 // Records a wait that gave up: the library's error word (W4A16_ERR_TIMEOUT) and the CTA's abort
 // flag, so the other roles stop waiting for work that will not come.
 __device__ __forceinline__ void raise_abort(volatile int* abort_flag, unsigned int* err) {
@@ -408,7 +429,7 @@ template <int W, int CH, int G, bool SWIGLU, typename L>
 __device__ __forceinline__ void issue_stage(const WeightMaps& wm, uint32_t code_dst,
                                             uint32_t scale_dst, uint32_t bar, int q, int cta_tile,
                                             int N, int z) {
-  constexpr int kT = W * CH;
+  constexpr int kT = L::kTiles;
   mbar_expect_tx(bar, L::kStageTx);
   if (wm.fast) {
     if constexpr (SWIGLU) {
@@ -640,7 +661,7 @@ __device__ __forceinline__ bool consumer_loop(char* base, int nq, int w, unsigne
     const int ngr = nq - c * CG < CG ? nq - c * CG : CG;
     const uint32_t fr = frag + b * L::kFragBytes;
     for (int q = 0; q < ngr; q += G) {
-      if (!wait_phase(bars.full + 8 * st, ph, abort_flag)) ok = false;
+      if (!wait_consumer(bars.full + 8 * st, ph, abort_flag)) ok = false;
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
