@@ -93,10 +93,47 @@ template <int NB, int W, int CH>
 using GeoB16 = ws::WsGeo<ws::kK1, NB, W, CH, 2,
                          (NB == 1 ? W4A16_B16_R : W4A16_B16B_R) * 16 / (W * CH),
                          NB == 1 ? 8 : W4A16_B16B_CG, 2>;
-constexpr int kN2W = W4A16_N2_W, kN2CH = 16 / W4A16_N2_W;
-constexpr int kK2aW = W4A16_K2A_W, kK2aCH = 16 / W4A16_K2A_W;
-constexpr int kK2bW = W4A16_K2B_W, kK2bCH = 16 / W4A16_K2B_W;
-constexpr int kB16W = W4A16_B16_W, kB16CH = 16 / W4A16_B16_W;
+#ifndef W4A16_N2_CH
+#define W4A16_N2_CH (16 / W4A16_N2_W)
+#endif
+#ifndef W4A16_K2A_CH
+#define W4A16_K2A_CH (16 / W4A16_K2A_W)
+#endif
+#ifndef W4A16_K2B_CH
+#define W4A16_K2B_CH (16 / W4A16_K2B_W)
+#endif
+#ifndef W4A16_B16_CH
+#define W4A16_B16_CH (16 / W4A16_B16_W)
+#endif
+constexpr int kN2W = W4A16_N2_W, kN2CH = W4A16_N2_CH;
+constexpr int kK2aW = W4A16_K2A_W, kK2aCH = W4A16_K2A_CH;
+constexpr int kK2bW = W4A16_K2B_W, kK2bCH = W4A16_K2B_CH;
+constexpr int kB16W = W4A16_B16_W, kB16CH = W4A16_B16_CH;
+// Resident CTAs per SM the launch bounds ask registers for: two where two fit in shared memory
+// (228 KB per SM, 1 KB reserved per CTA), else one.
+template <typename L>
+constexpr int min_blocks() {
+  return (2 * (L::kAlloc + 1024) <= 228 * 1024 && W4A16_MINB >= 2) ? 2 : 1;
+}
+// Split-K epilogue of geometry L: receive slots in shared memory of their own where they still
+// fit as many CTAs per SM as L alone (pushes then start as soon as a rank's stream ends), else in
+// the drained code ring (after a cluster barrier).
+template <typename L, bool SWIGLU>
+using SplitK = mma::SplitKPush<SWIGLU, L::kTiles * 32, L::MI::kRows>;
+template <typename L>
+constexpr int slots_off() {
+  return (L::kBytes + 127) / 128 * 128;
+}
+template <typename L, bool SWIGLU>
+constexpr bool own_slots() {
+  return min_blocks<L>() == 2
+             ? 2 * (L::kAlloc + 128 + SplitK<L, SWIGLU>::kSlotBytes + 1024) <= 228 * 1024
+             : L::kAlloc + 128 + SplitK<L, SWIGLU>::kSlotBytes <= 227 * 1024;
+}
+template <typename L, bool SWIGLU>
+constexpr int smem_bytes() {
+  return L::kAlloc + (own_slots<L, SWIGLU>() ? 128 + SplitK<L, SWIGLU>::kSlotBytes : 0);
+}
 
 // Output element stores: float32, or bf16 (bit pattern in uint16_t) rounded to nearest even.
 __device__ __forceinline__ void store4(float* y, float4 v) { *reinterpret_cast<float4*>(y) = v; }
@@ -121,7 +158,7 @@ __device__ __forceinline__ int slice_row0() {
 }
 
 template <typename L, bool SWIGLU, typename XT, typename YT>
-__global__ void __launch_bounds__(L::kThreads, W4A16_MINB)
+__global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
     ws_gemv_kernel(const __grid_constant__ WeightMaps wm, const __grid_constant__ CUtensorMap xmap,
                    YT* __restrict__ y, int M, int N, int K, unsigned int* err) {
   constexpr int MODE = L::kMode, NB = L::kNB, CH = L::kCH, G = L::kG;
@@ -146,6 +183,8 @@ __global__ void __launch_bounds__(L::kThreads, W4A16_MINB)
   ws::init_roles<L>(base);
   if (threadIdx.x == 0) ws::allow_dependents();
   __syncthreads();
+  constexpr bool kOwnSlots = own_slots<L, SWIGLU>();
+  if (kOwnSlots && CK > 1) mma::cluster_arrive_relaxed();  // barriers initialized, for the peers
   Acc<CH, NB> acc;
   int ex[LR::kN];
   if (warp == 0) {
@@ -195,9 +234,21 @@ __global__ void __launch_bounds__(L::kThreads, W4A16_MINB)
     return;
   }
   constexpr int kCols = kT * 32;
-  static_assert(L::MI::kRows * kCols * 4 <= L::kR * L::kCodeStage,
-                "split-K tile must fit in the code ring");
-  float* red = reinterpret_cast<float*>(base + L::kCodeOff);
+  using SK = SplitK<L, SWIGLU>;
+  static_assert(kOwnSlots || SK::kSlotBytes <= L::kR * L::kCodeStage,
+                "receive slots must fit in the code ring");
+  const ws::Bars<L> bars(base);
+  const uint32_t slots =
+      ws::smem_u32(base) + (kOwnSlots ? (uint32_t)slots_off<L>() : (uint32_t)L::kCodeOff);
+  if (!kOwnSlots) {
+    ws::fence_proxy_async_smem();  // the ring's generic reads, before the peers' async writes
+    mma::cluster_arrive();
+  }
+  // Own slots: every CTA of the cluster has started and initialized its receive barrier.
+  // Ring slots: every CTA's ring is drained.
+  mma::cluster_wait();
+  const SK sk(CK, rank, slots, bars.recv);
+  if (threadIdx.x == 0) ws::mbar_expect_tx(bars.recv, sk.rx_bytes(Ms));
   if (warp >= 2) {
 #pragma unroll
     for (int i = 0; i < LR::kN; ++i) {
@@ -214,12 +265,14 @@ __global__ void __launch_bounds__(L::kThreads, W4A16_MINB)
         } else {
           lc = 32 * (w * CH + c) + h4;
         }
-        *reinterpret_cast<float4*>(&red[m * kCols + lc]) =
-            ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f);
+        sk.put(m, lc, ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f));
       }
     }
   }
-  mma::cluster_finish<SWIGLU, kCols, YT>(cluster, red, blockIdx.x, Ms, N, y);
+  mma::cluster_arrive();  // this rank's sends are issued
+  if (!sk.finish(Ms, blockIdx.x, ldy, y) && threadIdx.x == 0)
+    ws::raise_abort(reinterpret_cast<volatile int*>(base + L::kAbortOff), err);
+  mma::cluster_wait();  // no CTA leaves while a peer may still send to it
 }
 
 // ------------------------------------------------------------------------------ host side
@@ -297,7 +350,7 @@ struct Instance {
   static constexpr auto kernel = ws_gemv_kernel<L, SWIGLU, XT, YT>;
 
   static cudaError_t data(const DeviceInfo& di, const LaunchData** ld) {
-    return launch_data(kernel, L::kAlloc, L::kThreads, cache, di, ld);
+    return launch_data(kernel, smem_bytes<L, SWIGLU>(), L::kThreads, cache, di, ld);
   }
   // Predicted fill of the GPU for this problem (see plan_split).
   static cudaError_t fill(int M, int N, int K, const DeviceInfo& di, double* eff) {
@@ -327,7 +380,7 @@ struct Instance {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(tiles, CK, nz);
     cfg.blockDim = dim3(L::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = L::kAlloc;
+    cfg.dynamicSmemBytes = smem_bytes<L, SWIGLU>();
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;

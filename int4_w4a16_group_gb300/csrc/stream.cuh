@@ -203,7 +203,7 @@ struct WsGeo {
   static constexpr int kFragOff = kXRawOff + 2 * kXRawBytes;
   static constexpr int kExpOff = kFragOff + 2 * kFragBytes;
   static constexpr int kBarOff = kExpOff + 2 * 32 * 4;
-  static constexpr int kNumBars = 2 * R + 6;
+  static constexpr int kNumBars = 2 * R + 7;  // + the split-K receive barrier
   static constexpr int kAbortOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kAbortOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base
@@ -460,13 +460,14 @@ __device__ __forceinline__ void issue_stage(const WeightMaps& wm, uint32_t code_
 // Barrier addresses of a CTA (see WsGeo).
 template <typename L>
 struct Bars {
-  uint32_t full, empty, xfull, ffull, fempty;
+  uint32_t full, empty, xfull, ffull, fempty, recv;
   __device__ __forceinline__ explicit Bars(char* base) {
     full = smem_u32(base + L::kBarOff);
     empty = full + L::kR * 8;
     xfull = empty + L::kR * 8;
     ffull = xfull + 16;
     fempty = ffull + 16;
+    recv = fempty + 16;
   }
 };
 
@@ -485,6 +486,7 @@ __device__ __forceinline__ void init_roles(char* base) {
       mbar_init(b.ffull + 8 * i, 32);
       mbar_init(b.fempty + 8 * i, L::kConsumers);
     }
+    mbar_init(b.recv, 1);
     *reinterpret_cast<volatile int*>(base + L::kAbortOff) = 0;
     mma::mbar_fence_init();
   }
