@@ -4,7 +4,7 @@
 Headline workload: the fused gate/up SwiGLU projection of a dense Kimi-K2-class MLP in decode /
 draft-tree verify, K = 7168, N = 2 x 18432, once for each of M = 1, 4 and 16 rows (one "pass":
 three launches, each streaming all 165.15 MB of packed weights and scales). One "step" is
---inner passes (400 by default), captured once as a CUDA graph and replayed, so the default 20
+--inner passes (480 by default), captured once as a CUDA graph and replayed, so the default 20
 timed steps last about a second. Metric: packed weight + scale bytes streamed from HBM per second
 (GB/s), and its fraction of the measured HBM copy bandwidth.
 
@@ -45,7 +45,7 @@ WORKLOAD = "dense SwiGLU gate+up decode, M in {1,4,16}, K=7168, N=2x18432, group
 M_LIST = (1, 4, 16)
 N_COPIES = 4
 BYTES_PER_WEIGHT = 0.625   # 0.5 B of packed code + 4 B scale / 32 weights
-INNER = 400                # passes of the three launches per timed step (>= 1 s at 20 steps)
+INNER = 480                # passes of the three launches per timed step (>= 1 s at 20 steps)
 BREAKDOWN_PASSES = 50      # eager passes with an event after every launch (per-M times)
 E2E_PASSES = 200           # end-to-end passes (host x in, host y out, synchronized each pass)
 ORACLE_PAIRS = 2048        # gate/up output pairs of the CPU-oracle sample (both CPU legs)
@@ -669,6 +669,15 @@ def profile_case(name: str):
             y = torch.empty((M, N // 2 if name == "gate_up" else N), device="cuda")
             t = _time_launches(stream, [lambda: fn(x, qw, sc, y, stream=stream)] * 3)
             out[f"M{M}_us"] = 1e3 * t[-1]
+    elif name == "gate_up_m64":
+        # four 16-row slices of one 165 MB weight copy: DRAM traffic shows whether the slices
+        # share the weight bytes through L2
+        K, N = synth.SWIGLU["K"], 2 * synth.SWIGLU["I"]
+        (qw, sc), = _quantized_copies(w4, K, N, 1, seed=5000)
+        x = synth.cuda_normal((64, K), 1.0, seed=64)
+        y = torch.empty((64, N // 2), device="cuda")
+        t = _time_launches(stream, [lambda: w4.w4a16_gemm_swiglu(x, qw, sc, y, stream=stream)] * 3)
+        out["M64_us"] = 1e3 * t[-1]
     elif name == "bf16_small":
         K, N = synth.PREFILL["K"], synth.PREFILL["N"]
         (qw, sc), = _quantized_copies(w4, K, N, 1, seed=5000)
@@ -721,7 +730,8 @@ def main(argv=None):
                     help="passes of the three launches per timed step (captured as one graph)")
     ap.add_argument("--copies", type=int, default=N_COPIES,
                     help="rotating weight copies of the headline workload (L2 defeat)")
-    ap.add_argument("--profile-case", choices=["gate_up", "down", "moe", "prefill", "bf16_small"],
+    ap.add_argument("--profile-case",
+                    choices=["gate_up", "gate_up_m64", "down", "moe", "prefill", "bf16_small"],
                     help="run one workload at ncu-capture size and exit")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -8,10 +8,10 @@
 // design goal is to stream every packed weight and scale byte exactly once with as few
 // instructions per weight as possible. The roles of a CTA live in stream.cuh.
 //
-// Grid: x = CTA column tiles (W consumer warps x CH 32-column tiles each), y = CK ranks of a
-// split over K (one thread-block cluster; partial tiles are added over distributed shared
-// memory in rank order: deterministic, no global scratch, no atomics), z = row slices of the
-// activations (16 rows each; one slice for M <= 16).
+// Grid: x = CTA column tiles (W consumer warps x CH 32-column tiles each) x row slices of the
+// activations (16 rows each, one for M <= 16; the slice index fastest), y = CK ranks of a split
+// over K (one thread-block cluster; partial tiles are sent to their owning rank over distributed
+// shared memory and added in rank order: deterministic, no global scratch, no atomics).
 #include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
@@ -83,8 +83,8 @@ using ws::WeightMaps;
 #endif
 // Ring depth scales with 16 / (tiles per CTA), so the narrow form keeps the wide form's bytes in
 // flight per CTA.
-template <int W, int CH>
-using GeoN2 = ws::WsGeo<ws::kN2, 1, W, CH, 2, W4A16_N2_R * 16 / (W * CH), 8, 4>;
+template <int W, int CH, int R = W4A16_N2_R * 16 / (W * CH)>
+using GeoN2 = ws::WsGeo<ws::kN2, 1, W, CH, 2, R, 8, 4>;
 template <int W, int CH>
 using GeoK2a = ws::WsGeo<ws::kK2, 1, W, CH, 2, W4A16_K2A_R * 16 / (W * CH), W4A16_K2A_CG, 4>;
 template <int W, int CH>
@@ -109,11 +109,13 @@ constexpr int kN2W = W4A16_N2_W, kN2CH = W4A16_N2_CH;
 constexpr int kK2aW = W4A16_K2A_W, kK2aCH = W4A16_K2A_CH;
 constexpr int kK2bW = W4A16_K2B_W, kK2bCH = W4A16_K2B_CH;
 constexpr int kB16W = W4A16_B16_W, kB16CH = W4A16_B16_CH;
-// Resident CTAs per SM the launch bounds ask registers for: two where two fit in shared memory
-// (228 KB per SM, 1 KB reserved per CTA), else one.
+// Resident CTAs per SM the launch bounds ask registers for: as many as fit in shared memory
+// (228 KB per SM, 1 KB reserved per CTA), at most W4A16_MINB.
+constexpr int fit_blocks(int smem) { return 228 * 1024 / (smem + 1024); }
 template <typename L>
 constexpr int min_blocks() {
-  return (2 * (L::kAlloc + 1024) <= 228 * 1024 && W4A16_MINB >= 2) ? 2 : 1;
+  return fit_blocks(L::kAlloc) < W4A16_MINB ? (fit_blocks(L::kAlloc) < 1 ? 1 : fit_blocks(L::kAlloc))
+                                            : W4A16_MINB;
 }
 // Split-K epilogue of geometry L: receive slots in shared memory of their own where they still
 // fit as many CTAs per SM as L alone (pushes then start as soon as a rank's stream ends), else in
@@ -126,9 +128,8 @@ constexpr int slots_off() {
 }
 template <typename L, bool SWIGLU>
 constexpr bool own_slots() {
-  return min_blocks<L>() == 2
-             ? 2 * (L::kAlloc + 128 + SplitK<L, SWIGLU>::kSlotBytes + 1024) <= 228 * 1024
-             : L::kAlloc + 128 + SplitK<L, SWIGLU>::kSlotBytes <= 227 * 1024;
+  return fit_blocks(L::kAlloc + 128 + SplitK<L, SWIGLU>::kSlotBytes) >= min_blocks<L>() &&
+         L::kAlloc + 128 + SplitK<L, SWIGLU>::kSlotBytes <= 227 * 1024;
 }
 template <typename L, bool SWIGLU>
 constexpr int smem_bytes() {
@@ -151,10 +152,17 @@ __device__ __forceinline__ float4 swiglu4(float4 g, float4 u) {
                      mma::silu_f(g.w) * u.w);
 }
 
-// Grid z = row slices of kRows rows: the slice's first row.
+// Grid x = column tile x row slice (kRows rows each), the slice index fastest: the slices of a
+// weight tile are resident together, so their copies of the same weight bytes meet in L2 and
+// the weights come from HBM once per launch whatever M is.
+struct GridPos {
+  int tile, row0;
+};
 template <typename L>
-__device__ __forceinline__ int slice_row0() {
-  return (int)blockIdx.z * L::MI::kRows;
+__device__ __forceinline__ GridPos grid_pos(int M) {
+  const int nz = (M + L::MI::kRows - 1) / L::MI::kRows;
+  const int tile = (int)blockIdx.x / nz;
+  return {tile, ((int)blockIdx.x - tile * nz) * L::MI::kRows};
 }
 
 template <typename L, bool SWIGLU, typename XT, typename YT>
@@ -169,7 +177,8 @@ __global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
   const int CK = (int)cluster.dim_blocks().y;
   const int rank = (int)cluster.block_index().y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
-  const int xrow0 = slice_row0<L>();
+  const GridPos gp = grid_pos<L>(M);
+  const int tile = gp.tile, xrow0 = gp.row0;
   const int Ms = min(M - xrow0, L::MI::kRows);
   const int ldy = SWIGLU ? N / 2 : N;
   y += (size_t)xrow0 * ldy;
@@ -191,7 +200,7 @@ __global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
     if (lane == 0) {
       ws::prefetch_tmap(&wm.codes);
       ws::prefetch_tmap(&wm.scales);
-      ws::producer_loop<SWIGLU, L>(wm, base, q0, nq, blockIdx.x, N, 0, err);
+      ws::producer_loop<SWIGLU, L>(wm, base, q0, nq, tile, N, 0, err);
     }
   } else if (warp == 1) {
     if (lane == 0) ws::prefetch_tmap(&xmap);
@@ -216,7 +225,7 @@ __global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
         constexpr int H = CH / 2;
 #pragma unroll
         for (int c = 0; c < H; ++c) {
-          const int j = 32 * (blockIdx.x * (kT / 2) + w * H + c) + h4;
+          const int j = 32 * (tile * (kT / 2) + w * H + c) + h4;
           if (j < ldy)
             store4(y + (size_t)m * ldy + j,
                    swiglu4(ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f),
@@ -225,7 +234,7 @@ __global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
       } else {
 #pragma unroll
         for (int c = 0; c < CH; ++c) {
-          const int col = 32 * (blockIdx.x * kT + w * CH + c) + h4;
+          const int col = 32 * (tile * kT + w * CH + c) + h4;
           if (col < N)
             store4(y + (size_t)m * N + col, ws::lane_result<MODE, CH, NB>(acc, c, b, odd, f));
         }
@@ -270,7 +279,7 @@ __global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
     }
   }
   mma::cluster_arrive();  // this rank's sends are issued
-  if (!sk.finish(Ms, blockIdx.x, ldy, y) && threadIdx.x == 0)
+  if (!sk.finish(Ms, tile, ldy, y) && threadIdx.x == 0)
     ws::raise_abort(reinterpret_cast<volatile int*>(base + L::kAbortOff), err);
   mma::cluster_wait();  // no CTA leaves while a peer may still send to it
 }
@@ -378,7 +387,7 @@ struct Instance {
     e = act_map<L, XT>(&xm, x, M, K);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(tiles, CK, nz);
+    cfg.gridDim = dim3(tiles * nz, CK, 1);
     cfg.blockDim = dim3(L::kThreads, 1, 1);
     cfg.dynamicSmemBytes = smem_bytes<L, SWIGLU>();
     cfg.stream = s;
@@ -424,7 +433,12 @@ cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* 
                      int K, const DeviceInfo& di, cudaStream_t s) {
   if (M <= 4) {
     using Wide = GeoN2<kN2W, kN2CH>;
-    using Narrow = GeoN2<narrow_w(kN2W, kN2CH, SWIGLU), narrow_ch(kN2W, kN2CH, SWIGLU)>;
+    constexpr int nw = narrow_w(kN2W, kN2CH, SWIGLU), nch = narrow_ch(kN2W, kN2CH, SWIGLU);
+#ifdef W4A16_N2_NRING
+    using Narrow = GeoN2<nw, nch, W4A16_N2_NRING>;
+#else
+    using Narrow = GeoN2<nw, nch>;
+#endif
     return launch_best<Instance<Wide, SWIGLU, float, float>, Instance<Narrow, SWIGLU, float, float>>(
         x, qw, sc, y, M, N, K, di, s);
   }

@@ -4,8 +4,9 @@
 // Unpack: (w & 0x000F000F) | 0x64006400 is the fp16 pair (1024 + nibble_0, 1024 + nibble_4); the
 // mask shifted by 4 gives 1024 + 16 * nibble; one fp16 FMA then yields nibble - 8 exactly. This
 // is the magic-number integer-to-float conversion (an integer OR'ed into the mantissa of a power
-// of two whose exponent makes the mantissa's last bit worth 1, then the power subtracted), the
-// published technique that mixed-precision GEMM kernels use for 4-bit weights.
+// of two whose exponent makes the mantissa's last bit worth 1, then the power subtracted), as
+// published for INT4/INT8-weight fp16 GEMMs by Kim et al., "Who Says Elephants Can't Run:
+// Bringing Large Scale MoE Models into Cloud Scale Production" (2022).
 //
 // MMA operand mapping (m16n8k16; g = lane / 4, t = lane % 4): A (16 x 16): rows = weight columns,
 // k = input index. Lane (g, t) holds the packed word of row 4q + t of group q for two columns

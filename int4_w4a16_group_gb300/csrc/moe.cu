@@ -533,7 +533,7 @@ cudaError_t launch_moe(const float* x, const int32_t* ids, const float* w, int T
 
 // The routed experts as in launch_moe, plus (when qs_gu is given) a shared expert that every
 // token goes through with weight 1: its gate/up + SwiGLU and down projections run as dense
-// small-M GEMMs (one launch each, 16-row slices as grid z) into the workspace, and the combine
+// small-M GEMMs (one launch each, all 16-row slices in its grid) into the workspace, and the combine
 // starts each row from it.
 cudaError_t launch_moe_block(const float* x, const int32_t* ids, const float* w, int T, int topk,
                              int E, const int32_t* qw_gu, const float* sc_gu,
