@@ -256,11 +256,12 @@ __device__ __forceinline__ uint4 frag_of(const float (&o)[8]) {
 
 // Converts raw chunk `buf` (ngr groups) into B fragments and row exponents. Lane (g, t) of the
 // prep warp writes exactly the 16-byte pieces consumer lane (g, t) will read.
-// Row exponents are sticky: a row keeps the exponent of earlier chunks (eprev) unless this
-// chunk's largest magnitude would not fit under it (fp16 holds up to 2^16 times 2^(e - 14), so
-// a chunk exponent up to e + 1 fits); the chunk's flag word tells the consumers whether any
-// row's exponent changed (only then do they rescale their accumulators). `first` starts a new
-// sequence of chunks.
+// Row exponents are sticky downwards: a row keeps the exponent e of earlier chunks (eprev)
+// while this chunk's largest magnitude is below 2^(e + 1), and takes the chunk's exponent when
+// it is larger. Scaled by 2^(14 - e) every value is then below 2^15, well inside fp16 (whose
+// largest finite value is 65504; round-to-nearest overflows from 65520, so a chunk one binade
+// up could not be kept). The chunk's flag word tells the consumers whether any row's exponent
+// changed (only then do they rescale their accumulators). `first` starts a new sequence.
 template <int MODE, int NB, typename XT, typename L>
 __device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr,
                                            int (&eprev)[MODE == kN2 ? 1 : NB], bool first) {
@@ -291,7 +292,7 @@ __device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr,
     amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
     const int ec = row_exponent(amax);
     // a row with no nonzero value so far takes the chunk's exponent
-    ex[i] = (first || eprev[i] == kNoExp || ec > eprev[i] + 1) ? ec : eprev[i];
+    ex[i] = (first || eprev[i] == kNoExp || ec > eprev[i]) ? ec : eprev[i];
     if (t == 0 && (MODE != kN2 || (g & 1) == 0)) fexp[rows[i]] = ex[i] == kNoExp ? 0 : ex[i];
   }
   bool changed = false;

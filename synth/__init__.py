@@ -65,6 +65,17 @@ def activations(M: int, K: int, seed=0, stream=2, std=1.0) -> np.ndarray:
     return normal((M, K), std, seed, stream)
 
 
+def packed_codes(K: int, N: int, seed=0, stream=6) -> np.ndarray:
+    """int32 [K/8, N] words of uniformly random bits: every packed 4-bit code uniform in 0..15."""
+    words = _rng(seed, stream).integers(0, 1 << 32, size=(K // 8, N), dtype=np.uint64)
+    return words.astype(np.uint32).view(np.int32)
+
+
+def group_scales(K: int, N: int, seed=0, stream=7, lo=0.002, hi=0.006) -> np.ndarray:
+    """float32 [K/32, N] positive scales drawn uniformly from [lo, hi)."""
+    return _rng(seed, stream).uniform(lo, hi, size=(K // 32, N)).astype(np.float32)
+
+
 def bf16_activations(M: int, K: int, seed=0, stream=3) -> np.ndarray:
     """bf16 activations ~ N(0,1), returned as their uint16 bit patterns [M, K].
 

@@ -105,6 +105,45 @@ def test_gemm_activation_range_along_k(w4, M):
         assert_close_rows(host(y), ref, FP32_TOL, f"range along K, M={M}, swiglu={swiglu}")
 
 
+def _top_of_binade_rows(M, K, seed):
+    """Rows of magnitude <= 1 (one value exactly 1) up to a switch point, then values <= 2 in
+    which every block of 64 inputs holds +-(4 - 2^-12): one binade above the start, in its top
+    2^-12. The switch points are staggered over the rows, so for any split over K some row
+    switches behind an activation-chunk boundary of its rank."""
+    x = synth.normal((M, K), 0.3, seed=seed, stream=2)
+    np.clip(x, -1.0, 1.0, out=x)
+    top = np.float32(4.0 - 2.0 ** -12)
+    for m in range(M):
+        s = 64 * (1 + 3 * m) % (K - 256) + 128
+        x[m, 0] = 1.0
+        x[m, s:] *= 2.0
+        x[m, s::64] = np.where(np.arange(len(x[m, s::64])) % 2 == 0, top, -top)
+    return x
+
+
+@pytest.mark.parametrize("M", [4, 16])
+def test_gemm_activation_top_of_binade(w4, M):
+    """A row's exponent may be kept while a later chunk's values are one binade larger; values in
+    the top 2^-12 of that binade must still fit the fp16 activation terms (no inf, float32
+    accuracy). Wide shapes keep the split over K small, so every rank sees several chunks."""
+    K, I = 2048, 18432
+    qw, sc = synth.packed_codes(K, 2 * I, seed=40 + M), synth.group_scales(K, 2 * I, seed=41 + M)
+    x = _top_of_binade_rows(M, K, seed=42 + M)
+    y = host(w4.w4a16_gemm_swiglu(dev(x), dev(qw), dev(sc)))
+    assert np.isfinite(y).all(), "non-finite gate/up output"
+    cols = np.sort(np.random.default_rng(43 + M).choice(I, 384, replace=False))
+    both = np.concatenate([cols, I + cols])
+    ref = oracle.swiglu_gemm(x, qw[:, both], sc[:, both])
+    assert_close_rows(y[:, cols], ref, FP32_TOL, f"gate/up top of binade, M={M}")
+    K, N = 4096, 18432
+    qw, sc = synth.packed_codes(K, N, seed=44 + M), synth.group_scales(K, N, seed=45 + M)
+    x = _top_of_binade_rows(M, K, seed=46 + M)
+    y = host(w4.w4a16_gemm(dev(x), dev(qw), dev(sc)))
+    assert np.isfinite(y).all(), "non-finite plain output"
+    ref = oracle.gemm(x, qw[:, cols], sc[:, cols])
+    assert_close_rows(y[:, cols], ref, FP32_TOL, f"plain top of binade, M={M}")
+
+
 def test_gemm_zero_weights_and_empty(w4):
     K, N = 256, 128
     qw, sc = oracle.quantize_w4a16(np.zeros((K, N), dtype=np.float32))
