@@ -12,7 +12,10 @@ Timing: W warm-up steps, then K timed steps bracketed by a barrier and a device 
 CUDA events on the launching stream, max over ranks. Each launch reads a different one of
 four weight copies (660 MB in total, > 5x the 129 MB L2), so no launch finds its weights in L2.
 SM clocks are sampled with nvidia-smi during the timed region. The roofline object reports the
-kernel with the largest share of a pass (per-launch CUDA events over 50 eager passes).
+kernel with the largest share of a pass, timed as 160 back-to-back launches of its M captured as
+one graph (per_M_stream; the three per-M stream times add up to the step's time per pass).
+per_M gives each M's isolated launch time (an event after every launch of 50 eager passes,
+which adds each launch's gap to the next).
 
 Also reported, outside the step: the down projection (K=18432, N=7168), the routed MoE block
 (T=64, E=384, top-8), the large-M bf16 contraction, bf16 activations at small M, an M sweep of
@@ -47,6 +50,7 @@ N_COPIES = 4
 BYTES_PER_WEIGHT = 0.625   # 0.5 B of packed code + 4 B scale / 32 weights
 INNER = 480                # passes of the three launches per timed step (>= 1 s at 20 steps)
 BREAKDOWN_PASSES = 50      # eager passes with an event after every launch (per-M times)
+STREAM_LAUNCHES = 160      # per-M graph of back-to-back launches of one M (per-M stream times)
 E2E_PASSES = 200           # end-to-end passes (host x in, host y out, synchronized each pass)
 ORACLE_PAIRS = 2048        # gate/up output pairs of the CPU-oracle sample (both CPU legs)
 SWEEP_M = (16, 24, 32, 48, 64, 128, 256, 512)   # rows of the decode-to-prefill sweep
@@ -242,6 +246,29 @@ def _time_region(stream, fns):
     return a.elapsed_time(b)
 
 
+def _graph_us(call, n):
+    """Microseconds per call of n back-to-back calls captured as one CUDA graph (call(i, s)
+    issues call i on stream s), timed with CUDA events around one replay after two warm-up
+    replays: the calls overlap their neighbours' launch and prologue as in a serving loop."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        s = torch.cuda.current_stream()
+        for i in range(n):
+            call(i, s)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    cur = torch.cuda.current_stream()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(cur)
+    g.replay()
+    b.record(cur)
+    torch.cuda.synchronize()
+    del g
+    return 1e3 * a.elapsed_time(b) / n
+
+
 def run_ours(args, rank, world):
     import torch
     import int4_w4a16_group_gb300 as w4
@@ -320,6 +347,20 @@ def run_ours(args, rank, world):
                       "frac_of_hbm": wbytes / (statistics.median(per_launch[M]) * 1e-3) / 1e9 / peaks["hbm_gbs"]}
              for M in M_LIST}
 
+    # per-M stream times: one CUDA graph per M of STREAM_LAUNCHES back-to-back launches of that
+    # M alone (rotating weight copies, as in the step), events around the replay: each kernel's
+    # average launch duration as it runs in the step (launches overlapping their neighbours'
+    # launch and prologue), free of the gaps that an event after every launch adds.
+    per_m_stream = {}
+    for M in M_LIST:
+        us = _graph_us(lambda i, s_, M=M: w4.w4a16_gemm_swiglu(
+            xs[M], weights[i % n_copies][0], weights[i % n_copies][1], ys[M], stream=s_),
+            STREAM_LAUNCHES)
+        per_m_stream[str(M)] = {"us": us, "GB/s": wbytes / (us * 1e-6) / 1e9,
+                                "frac_of_hbm": wbytes / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+    pass_us = 1e3 * ms_per_step / inner
+    stream_sum_us = sum(v["us"] for v in per_m_stream.values())
+
     # end to end through the public API: pinned host x in, host y out, every step
     xh = {M: torch.empty((M, K), dtype=torch.float32, pin_memory=True).copy_(xs[M].cpu()) for M in M_LIST}
     yh = {M: torch.empty((M, I), dtype=torch.float32, pin_memory=True) for M in M_LIST}
@@ -388,8 +429,8 @@ def run_ours(args, rank, world):
            "method": e2e_method + "; each pass copies its own x in and y out",
            "eager_value": world * E2E_PASSES * len(M_LIST) * wbytes / e2e_eager_s / 1e9}
     del weights
-    dom = max(M_LIST, key=lambda M: per_m[str(M)]["us"])  # the kernel with the largest time share
-    dom_gbs = per_m[str(dom)]["GB/s"]
+    dom = max(M_LIST, key=lambda M: per_m_stream[str(M)]["us"])  # largest time share of a pass
+    dom_gbs = per_m_stream[str(dom)]["GB/s"]
 
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -398,6 +439,9 @@ def run_ours(args, rank, world):
         "data": "synthetic (seeded N(0,0.02) weights quantized on the device, N(0,1) activations)",
         "config": bench_config(world, n_copies, inner),
         "per_M": per_m,
+        "per_M_stream": per_m_stream,
+        "stream_sum_check": {"pass_us": pass_us, "sum_of_per_M_stream_us": stream_sum_us,
+                             "ratio": stream_sum_us / pass_us},
         "step_mean_GB/s": achieved,
         "roofline": {"bound": "hbm", "achieved": dom_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": dom_gbs / peaks["hbm_gbs"],
@@ -405,8 +449,11 @@ def run_ours(args, rank, world):
                      "kernel": f"w4a16 small-M weight-streaming GEMM, fused SwiGLU, M={dom} "
                                "(the largest time share of the step)",
                      "algorithmic_bytes_per_launch": wbytes,
-                     "timing": f"median of {BREAKDOWN_PASSES} launches, CUDA events on the "
-                               "launching stream, after the timed region",
+                     "timing": f"{STREAM_LAUNCHES} back-to-back launches of this M captured as "
+                               "one CUDA graph (as in the step), CUDA events on the launching "
+                               "stream around the replay, after the timed region; the three "
+                               "per-M stream times add up to the step's time per pass "
+                               "(stream_sum_check)",
                      "peak_source": peaks["source"] + " hbm_gbs (copy)"},
         "clocks": clocks,
         "e2e": e2e,
@@ -419,7 +466,8 @@ def run_ours(args, rank, world):
 
 def other_workloads(args, w4, peaks, stream):
     """Down projection, routed MoE, large-M bf16 and tiny: each timed on its own (not part of
-    the step), device time per launch with CUDA events, after warm-up."""
+    the step), device time per launch with CUDA events, after warm-up ("us": an event after
+    every launch; "stream_us" where given: back-to-back launches captured as one graph)."""
     import torch
     import synth
     res = {}
@@ -437,8 +485,11 @@ def other_workloads(args, w4, peaks, stream):
                                          stream=stream) for c in range(reps + 3)]
         t = _time_launches(stream, fns)[3:]
         us = 1e3 * statistics.mean(t)
+        su = _graph_us(lambda i, s_: w4.w4a16_gemm(x, copies[i % N_COPIES][0],
+                                                   copies[i % N_COPIES][1], y, stream=s_), 80)
         down[str(M)] = {"us": us, "GB/s": wb / (us * 1e-6) / 1e9,
-                        "frac_of_hbm": wb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+                        "frac_of_hbm": wb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                        "stream_us": su, "stream_frac_of_hbm": wb / (su * 1e-6) / 1e9 / peaks["hbm_gbs"]}
     res["down_K18432_N7168"] = down
     del copies
 
@@ -537,8 +588,11 @@ def other_workloads(args, w4, peaks, stream):
                                               yb, stream=stream) for c in range(reps + 3)]
         t = _time_launches(stream, fns)[3:]
         us = 1e3 * statistics.mean(t)
+        su = _graph_us(lambda i, s_: w4.w4a16_gemm_bf16(xb, copies[i % N_COPIES][0],
+                                                        copies[i % N_COPIES][1], yb, stream=s_), 80)
         b16[str(M)] = {"us": us, "GB/s": wb / (us * 1e-6) / 1e9,
-                       "frac_of_hbm": wb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"]}
+                       "frac_of_hbm": wb / (us * 1e-6) / 1e9 / peaks["hbm_gbs"],
+                       "stream_us": su, "stream_frac_of_hbm": wb / (su * 1e-6) / 1e9 / peaks["hbm_gbs"]}
     res["bf16_small_M_K7168_N18432"] = b16
 
     # M sweep between decode and prefill (same weights): float32 activations through w4a16_gemm

@@ -76,10 +76,14 @@ using ws::WeightMaps;
 #ifndef W4A16_MINB
 #define W4A16_MINB 2
 #endif
-// Launch with programmatic stream serialization: a launch may overlap the tail of the previous
-// kernel on its stream (only the activation loads wait for it).
+// Launch with programmatic stream serialization (1): a launch may then overlap the tail of the
+// previous kernel on its stream (only the activation loads wait for it). Off by default: the
+// next grid's clusters are then placed into the slots the previous grid frees one by one, and
+// when a grid needs every cluster slot of the GPU (e.g. 36 clusters of 8 CTAs) the last of its
+// clusters find no room until its own CTAs exit: a second wave that costs more (up to +60 % per
+// launch back to back) than the overlap saves (0.3 - 0.5 us per launch where it fits).
 #ifndef W4A16_PDL
-#define W4A16_PDL 1
+#define W4A16_PDL 0
 #endif
 // Ring depth scales with 16 / (tiles per CTA), so the narrow form keeps the wide form's bytes in
 // flight per CTA.

@@ -215,13 +215,16 @@ struct WsGeo {
 
 // ------------------------------------------------------------------------------ prep warp
 
-// Exponent of a row's largest magnitude (|x| < 2^(e+1)), clamped so that 2^(14 - e) and the
-// result factors stay normal floats; kNoExp for an all-zero row.
+// Exponent of a row's largest magnitude (|x| < 2^(e+1)); kNoExp for an all-zero row. Every
+// finite float32 has e <= 127, so scaled by 2^(14 - e) it stays below 2^15. The lower clamp
+// keeps 2^(14 - e), the output factor 2^(e - 14) and the rescale factors between chunks
+// (two halves of 2^(e_old - e_new)) normal floats; rows whose largest magnitude is below
+// 2^-100 are scaled as if it were 2^-100 and keep fewer significant bits.
 constexpr int kNoExp = -1000;
 __device__ __forceinline__ int row_exponent(float amax) {
   if (amax == 0.0f) return kNoExp;
   const int ex = (int)((__float_as_uint(amax) >> 23) & 0xFF) - 127;
-  return ex < -100 ? -100 : (ex > 100 ? 100 : ex);
+  return ex < -100 ? -100 : ex;
 }
 
 __device__ __forceinline__ float load_act(const float* p) { return *p; }

@@ -144,6 +144,23 @@ def test_gemm_activation_top_of_binade(w4, M):
     assert_close_rows(y[:, cols], ref, FP32_TOL, f"plain top of binade, M={M}")
 
 
+def test_gemm_activation_magnitude_limits(w4):
+    """Rows near the ends of the float32 range: ~2^110, ~2^-95, and one that falls from 2^100 to
+    2^-80 along K (the exponent stays at the large part; the small part's contribution is far
+    below float32 resolution of the result)."""
+    K, N = 2048, 520
+    W = synth.weights(K, N, seed=51, outliers=True)
+    x = synth.activations(4, K, seed=52)
+    x[0] *= np.float32(2.0 ** 110)
+    x[1] *= np.float32(2.0 ** -95)
+    x[2, : K // 2] *= np.float32(2.0 ** 100)
+    x[2, K // 2:] *= np.float32(2.0 ** -80)
+    qo, so = oracle.quantize_w4a16(W)
+    y = host(w4.w4a16_gemm(dev(x), dev(qo), dev(so)))
+    assert np.isfinite(y).all()
+    assert_close_rows(y, oracle.gemm(x, qo, so), FP32_TOL, "magnitude limits")
+
+
 def test_gemm_zero_weights_and_empty(w4):
     K, N = 256, 128
     qw, sc = oracle.quantize_w4a16(np.zeros((K, N), dtype=np.float32))
