@@ -282,10 +282,13 @@ __global__ void __launch_bounds__(L::kThreads, min_blocks<L>())
       }
     }
   }
-  mma::cluster_arrive();  // this rank's sends are issued
+  // This rank's sends are issued. Relaxed: an owner learns that its data has landed from its
+  // receive barrier (the sends' byte counts complete it with release semantics), so this arrive
+  // need not wait for the stores to be performed at the peers.
+  mma::cluster_arrive_relaxed();
   if (!sk.finish(Ms, tile, ldy, y) && threadIdx.x == 0)
     ws::raise_abort(reinterpret_cast<volatile int*>(base + L::kAbortOff), err);
-  mma::cluster_wait();  // no CTA leaves while a peer may still send to it
+  mma::cluster_wait();  // every peer has issued its sends: none is still to come
 }
 
 // ------------------------------------------------------------------------------ host side

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import FP32_TOL, assert_close_rows, dev, host, lib
+from gpu_util import BF16_TOL, FP32_TOL, assert_close_rows, dev, host, lib
 
 pytestmark = pytest.mark.gpu
 
@@ -48,7 +48,7 @@ def test_dequantize_bit_exact_every_nibble(w4):
 
 # ----------------------------------------------------------------------------- GEMM
 
-@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 33, 100])
+@pytest.mark.parametrize("M", [1, 2, 3, 4, 5, 8, 15, 16, 17, 33, 64, 100, 300])
 @pytest.mark.parametrize("K,N", [(512, 1000), (2048, 260)])
 def test_gemm_small(w4, M, K, N):
     W = synth.weights(K, N, seed=M + K, outliers=True)
@@ -161,6 +161,36 @@ def test_gemm_activation_magnitude_limits(w4):
     assert_close_rows(y, oracle.gemm(x, qo, so), FP32_TOL, "magnitude limits")
 
 
+def test_launches_replayed_from_a_cuda_graph(w4):
+    """The streaming GEMMs captured in one CUDA graph (as the bench step and a serving loop issue
+    them: float32 gate/up at M = 1, 4, 16 and a bf16 call back to back on one stream) and
+    replayed twice give the oracle's results."""
+    K, I = 2048, 1040
+    W = synth.weights(K, 2 * I, seed=61)
+    qo, so = oracle.quantize_w4a16(W)
+    q, s = dev(qo), dev(so)
+    xs = {M: synth.activations(M, K, seed=62 + M) for M in (1, 4, 16)}
+    xd = {M: dev(x) for M, x in xs.items()}
+    ys = {M: torch.zeros((M, I), dtype=torch.float32, device="cuda") for M in xs}
+    bits = synth.bf16_activations(8, K, seed=66)
+    xb = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    yb = torch.zeros((8, 2 * I), dtype=torch.bfloat16, device="cuda")
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        cs = torch.cuda.current_stream()
+        for M in (16, 4, 1):
+            w4.w4a16_gemm_swiglu(xd[M], q, s, ys[M], stream=cs)
+        w4.w4a16_gemm_bf16(xb, q, s, yb, stream=cs)
+    for _ in range(2):
+        g.replay()
+    torch.cuda.synchronize()
+    for M, x in xs.items():
+        assert_close_rows(host(ys[M]), oracle.swiglu_gemm(x, qo, so), FP32_TOL, f"graph M={M}")
+    yb64 = yb.float().cpu().numpy().astype(np.float64)
+    assert_close_rows(yb64, oracle.gemm_bf16(bits, qo, so), BF16_TOL, "graph bf16")
+    assert w4.w4a16_device_error() == 0
+
+
 def test_gemm_zero_weights_and_empty(w4):
     K, N = 256, 128
     qw, sc = oracle.quantize_w4a16(np.zeros((K, N), dtype=np.float32))
@@ -183,7 +213,7 @@ def test_gemm_is_deterministic(w4):
 
 # ----------------------------------------------------------------------------- SwiGLU
 
-@pytest.mark.parametrize("M", [1, 2, 4, 7, 16, 20, 64])
+@pytest.mark.parametrize("M", [1, 2, 4, 7, 16, 20, 64, 300])
 @pytest.mark.parametrize("K,I", [(1024, 520), (256, 64)])
 def test_swiglu_small(w4, M, K, I):
     W = synth.weights(K, 2 * I, seed=M + I)
