@@ -84,7 +84,9 @@ w4a16_status w4a16_dequantize(const int32_t* qw, const float* sc, int K, int N, 
  * Inference Engine", section "The Multi-Step Integration Chain", step 1; page "The Weight of
  * Precision ...", section "The Kernel: w4a16_gemm".
  * Any M >= 0; the kernels are built for the decode / draft-tree-verify regime (M <= 16):
- * larger M runs as 16-row slices within one launch. Deterministic (fixed reduction order). */
+ * larger M runs as 16-row slices within one launch, the slices of a weight tile resident
+ * together so each weight byte comes from HBM once per call. Deterministic (fixed reduction
+ * order). */
 w4a16_status w4a16_gemm(const float* x, const int32_t* qw, const float* sc, float* y,
                         int M, int N, int K, int group, w4a16_stream_t stream);
 

@@ -34,9 +34,13 @@ using ws::WeightMaps;
 //   up to 4 rows (two-term columns): 512 or 256 columns per CTA;
 //   5..8 rows and 9..16 rows (terms summed over k): 512 or 256 columns;
 //   bf16 activations (one term): 512 or 256 columns.
-// Compile-time knobs (consumer warps of the wide form, ring stages, chunk groups per mode); the
-// defaults are the measured best on GB300. The wide form has 16 tiles (512 columns) per CTA, the
-// narrow form 8 tiles with half the warps; both keep CH = 16 / W tiles per warp.
+// Compile-time knobs per form: consumer warps (_W), tiles per warp (_CH, default 16 / W), ring
+// depth (_R, scaled by 16 / tiles so every form keeps 16 tiles' worth of stages in flight),
+// activation chunk groups (_CG); W4A16_N2_NRING sets the narrow <= 4-row ring directly,
+// W4A16_MINB caps the CTAs per SM the launch bounds ask registers for, W4A16_PDL turns on
+// programmatic dependent launch. The defaults are the measured best on GB300. The wide form has
+// 16 tiles (512 columns) per CTA, the narrow form 8: the same warps with half the tiles each, or
+// half the warps where a fused SwiGLU warp needs its gate/up pair.
 #ifndef W4A16_N2_W
 #define W4A16_N2_W 4
 #endif

@@ -2,15 +2,12 @@
 // sums of the same output tile over different K ranges and add them through distributed shared
 // memory in rank order (deterministic, no global scratch, no atomics).
 #pragma once
-#include <cooperative_groups.h>
 #include <cuda_bf16.h>
 
 #include "mma_core.cuh"
 
 namespace w4a16 {
 namespace mma {
-
-namespace cg = cooperative_groups;
 
 // Output element stores: float32, or bf16 (bit pattern in uint16_t) rounded to nearest even.
 __device__ __forceinline__ void store_out(float* y, size_t i, float v) { y[i] = v; }

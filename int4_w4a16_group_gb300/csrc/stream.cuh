@@ -9,8 +9,9 @@
 //
 // A CTA has three roles:
 //   * producer warp (one elected lane): per stage of G groups (4G packed rows) one TMA copy of
-//     the codes of all the CTA's 32-column tiles (a 3-D/4-D box: columns x rows x tiles
-//     [x gate/up half]) and one of their scales, into an R-stage ring (full/empty mbarriers);
+//     the codes of all the CTA's 32-column tiles (a 4-D/5-D box: columns x rows x tiles
+//     [x gate/up half] x matrix, the last coordinate picking an expert of stacked MoE weights)
+//     and one of their scales, into an R-stage ring (full/empty mbarriers);
 //   * prep warp: TMA-loads raw activation chunks (CG groups x up to 16 rows), finds each row's
 //     largest magnitude in the chunk, and writes the rows as MMA B-fragments in fp16: the row
 //     scaled by 2^(14 - e) (e = the row's exponent in this chunk) split into hi + lo terms, 22
@@ -422,8 +423,9 @@ __device__ __forceinline__ float4 lane_result(const Acc<CH, NB>& acc, int c, int
 // ------------------------------------------------------------------------------ producer
 
 // Weight operands of one launch: the fast form copies all of a CTA's tiles of a stage with one
-// 3-D (plain) or 4-D (gate/up halves) box; the fallback (N or N/2 not a multiple of 32) copies
-// one 32-column 2-D box per tile, with columns past the matrix read as zero.
+// 4-D (plain) or 5-D (gate/up halves) box, the last coordinate selecting the matrix (an expert
+// of stacked MoE weights; 0 for a dense GEMM); the fallback (N or N/2 not a multiple of 32)
+// copies one 32-column 3-D box per tile, with columns past the matrix read as zero.
 struct WeightMaps {
   CUtensorMap codes, scales;
   int fast;  // 1: multi-tile boxes; 0: per-tile boxes
