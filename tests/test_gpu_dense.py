@@ -191,6 +191,48 @@ def test_launches_replayed_from_a_cuda_graph(w4):
     assert w4.w4a16_device_error() == 0
 
 
+@pytest.mark.parametrize("M", [1, 16])
+def test_gemm_split_over_k_for_every_tile_count(w4, M):
+    """1 to 20 wide column tiles at K = 8192: the launch planner splits K over clusters of
+    whatever size fills the GPU for each count (1 to 16 CTAs), so the split-K sends, receive
+    slots and rank-ordered sums run for most cluster sizes. Sampled columns (first, last and a
+    seeded spread) against the oracle."""
+    K = 8192
+    x = synth.activations(M, K, seed=70 + M)
+    for T in range(1, 21):
+        N = 512 * T
+        qw = synth.packed_codes(K, N, seed=71 + T)
+        sc = synth.group_scales(K, N, seed=72 + T)
+        y = host(w4.w4a16_gemm(dev(x), dev(qw), dev(sc)))
+        rng = np.random.default_rng(73 + T)
+        cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 62, replace=False)]))
+        assert_close_rows(y[:, cols], oracle.gemm(x, qw[:, cols], sc[:, cols]), FP32_TOL,
+                          f"split over K, M={M}, {T} tiles")
+    assert w4.w4a16_device_error() == 0
+
+
+def test_gemm_on_two_streams_at_once(w4):
+    """Two streams each issue gate/up GEMMs while the other runs: both match the oracle (the
+    per-device launch data is shared; nothing else is)."""
+    K, I = 2048, 1040
+    W = synth.weights(K, 2 * I, seed=81)
+    qo, so = oracle.quantize_w4a16(W)
+    q, s = dev(qo), dev(so)
+    xs = [synth.activations(M, K, seed=82 + M) for M in (4, 16)]
+    xd = [dev(x) for x in xs]
+    ys = [torch.empty((x.shape[0], I), dtype=torch.float32, device="cuda") for x in xs]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(8):
+        for j in range(2):
+            w4.w4a16_gemm_swiglu(xd[j], q, s, ys[j], stream=streams[j])
+    torch.cuda.synchronize()
+    for j in range(2):
+        assert_close_rows(host(ys[j]), oracle.swiglu_gemm(xs[j], qo, so), FP32_TOL,
+                          f"stream {j}")
+    assert w4.w4a16_device_error() == 0
+
+
 def test_gemm_zero_weights_and_empty(w4):
     K, N = 256, 128
     qw, sc = oracle.quantize_w4a16(np.zeros((K, N), dtype=np.float32))
