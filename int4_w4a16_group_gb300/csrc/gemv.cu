@@ -89,6 +89,16 @@ using ws::WeightMaps;
 #ifndef W4A16_PDL
 #define W4A16_PDL 0
 #endif
+// The narrow form is launched only when it fills the GPU this many times better than the wide;
+// the <= 4-row form has its own margin (down, N = 7168: 224 wide CTAs streamed faster than 280
+// narrow ones, 19.9 against 20.4 us back to back; at 16 rows the narrow ones won, 37.1 against
+// 39.0 us).
+#ifndef W4A16_NARROW_MARGIN
+#define W4A16_NARROW_MARGIN 1.03
+#endif
+#ifndef W4A16_N2_NARROW_MARGIN
+#define W4A16_N2_NARROW_MARGIN 1.3
+#endif
 // Ring depth scales with 16 / (tiles per CTA), so the narrow form keeps the wide form's bytes in
 // flight per CTA.
 template <int W, int CH, int R = W4A16_N2_R * 16 / (W * CH)>
@@ -418,18 +428,19 @@ template <typename L, bool SWIGLU, typename XT, typename YT>
 LaunchCache Instance<L, SWIGLU, XT, YT>::cache;
 
 // Of two geometries (wide: more columns per CTA, narrow: fewer), launches the wide one unless the
-// narrow one fills the GPU more than 3 % better. Wide CTAs share each activation fragment
-// between more columns.
+// narrow one fills the GPU more than `margin` times better. Wide CTAs share each activation
+// fragment and each stage's fixed work between more columns.
 template <typename Wide, typename Narrow, typename XT, typename YT>
 cudaError_t launch_best(const XT* x, const int32_t* qw, const float* sc, YT* y, int M, int N,
-                        int K, const DeviceInfo& di, cudaStream_t s) {
+                        int K, const DeviceInfo& di, cudaStream_t s,
+                        double margin = W4A16_NARROW_MARGIN) {
   double ew = 0.0, en = 0.0;
   cudaError_t e = Wide::fill(M, N, K, di, &ew);
   if (e != cudaSuccess) return e;
   e = Narrow::fill(M, N, K, di, &en);
   if (e != cudaSuccess) return e;
-  return ew * 1.03 >= en ? Wide::launch(x, qw, sc, y, M, N, K, di, s)
-                         : Narrow::launch(x, qw, sc, y, M, N, K, di, s);
+  return ew * margin >= en ? Wide::launch(x, qw, sc, y, M, N, K, di, s)
+                           : Narrow::launch(x, qw, sc, y, M, N, K, di, s);
 }
 
 // The narrow form (8 tiles per CTA) of a wide geometry with W warps of CH tiles: the same warps
@@ -451,7 +462,7 @@ cudaError_t dispatch(const float* x, const int32_t* qw, const float* sc, float* 
     using Narrow = GeoN2<nw, nch>;
 #endif
     return launch_best<Instance<Wide, SWIGLU, float, float>, Instance<Narrow, SWIGLU, float, float>>(
-        x, qw, sc, y, M, N, K, di, s);
+        x, qw, sc, y, M, N, K, di, s, W4A16_N2_NARROW_MARGIN);
   }
   if (M <= 8) {
     using Wide = GeoK2a<kK2aW, kK2aCH>;
