@@ -211,6 +211,25 @@ def test_gemm_split_over_k_for_every_tile_count(w4, M):
     assert w4.w4a16_device_error() == 0
 
 
+@pytest.mark.parametrize("M", [1, 8, 16])
+def test_bf16_split_over_k_for_every_tile_count(w4, M):
+    """The bf16 one-term forms over 1 to 20 wide column tiles at K = 8192 (cluster sizes 1 to 16,
+    receive slots of their own or in the code ring): sampled columns against the exact product."""
+    K = 8192
+    bits = synth.bf16_activations(M, K, seed=90 + M)
+    xb = torch.from_numpy(bits.view(np.int16)).cuda().view(torch.bfloat16)
+    for T in range(1, 21):
+        N = 512 * T
+        qw = synth.packed_codes(K, N, seed=91 + T)
+        sc = synth.group_scales(K, N, seed=92 + T)
+        y = w4.w4a16_gemm_bf16(xb, dev(qw), dev(sc)).float().cpu().numpy().astype(np.float64)
+        rng = np.random.default_rng(93 + T)
+        cols = np.unique(np.concatenate([[0, N - 1], rng.choice(N, 62, replace=False)]))
+        assert_close_rows(y[:, cols], oracle.gemm_bf16(bits, qw[:, cols], sc[:, cols]), BF16_TOL,
+                          f"bf16 split over K, M={M}, {T} tiles")
+    assert w4.w4a16_device_error() == 0
+
+
 def test_gemm_on_two_streams_at_once(w4):
     """Two streams each issue gate/up GEMMs while the other runs: both match the oracle (the
     per-device launch data is shared; nothing else is)."""
