@@ -191,7 +191,7 @@ def test_launches_replayed_from_a_cuda_graph(w4):
     assert w4.w4a16_device_error() == 0
 
 
-@pytest.mark.parametrize("M", [1, 16])
+@pytest.mark.parametrize("M", [1, 8, 16])
 def test_gemm_split_over_k_for_every_tile_count(w4, M):
     """1 to 20 wide column tiles at K = 8192: the launch planner splits K over clusters of
     whatever size fills the GPU for each count (1 to 16 CTAs), so the split-K sends, receive
