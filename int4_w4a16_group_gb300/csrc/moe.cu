@@ -321,8 +321,8 @@ __device__ __forceinline__ void moe_consumers(char* base, const GroupedArgs& a, 
         ok = false;
         break;
       }
-      const bool changed = cj == 0 || fexp[32 * b + 16] != 0;
-      const int en = changed ? fexp[32 * b + t] : ex;
+      const bool changed = cj == 0 || fexp[L::kExpInts * b + L::kExpFlag] != 0;
+      const int en = changed ? fexp[L::kExpInts * b + t] : ex;
       if (cj > 0 && changed) {
         const int d = ex - en;
         const float f = mma::exp2i(d >> 1) * mma::exp2i(d - (d >> 1));

@@ -175,7 +175,7 @@ struct ModeInfo {
 //   scales R stages x kTiles x (G x 128 B)
 //   xraw   2 x (kRows x 32 CG activations)         -- raw activation chunks (TMA)
 //   frag   2 x (CG x kFragGroup)                   -- prepared B fragments
-//   fexp   2 x 32 ints                             -- row exponents (16) and a changed flag
+//   fexp   2 x kExpInts ints                       -- row exponents (up to 32) and a changed flag
 //   bars   full[R], empty[R], xfull[2], ffull[2], fempty[2]; abort flag
 // CG = groups per activation chunk (at most 8: a TMA box row holds at most 256 elements).
 template <int MODE, int NB, int W, int CH, int G, int R, int CG, int XBYTES>
@@ -203,12 +203,15 @@ struct WsGeo {
   static constexpr int kXRawOff = kScaleOff + R * kScaleStage;
   static constexpr int kFragOff = kXRawOff + 2 * kXRawBytes;
   static constexpr int kExpOff = kFragOff + 2 * kFragBytes;
-  static constexpr int kBarOff = kExpOff + 2 * 32 * 4;
+  static constexpr int kExpInts = 64;  // per buffer: row exponents [0, 32), changed flag at 32
+  static constexpr int kExpFlag = 32;
+  static constexpr int kBarOff = kExpOff + 2 * kExpInts * 4;
   static constexpr int kNumBars = 2 * R + 7;  // + the split-K receive barrier
   static constexpr int kAbortOff = kBarOff + kNumBars * 8;
   static constexpr int kBytes = kAbortOff + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base
   static_assert(G % 2 == 0, "a tile's rows must fill whole 1 KB swizzle periods");
+  static_assert(MI::kRows <= kExpFlag, "row exponents must fit below the changed flag");
   static_assert(CG % G == 0 && CG <= 8, "a chunk is a whole number of stages, <= 256 inputs");
   static_assert((kCodeStage % 1024) == 0 && (kScaleOff % 1024) == 0, "TMA destinations");
   static_assert((kXRawOff % 128) == 0 && (kFragOff % 128) == 0, "16-byte aligned buffers");
@@ -274,7 +277,7 @@ __device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr,
   constexpr int kRowBytes = L::kCG * 32 * (int)sizeof(XT);
   const uint32_t raw = smem_u32(base + L::kXRawOff + buf * L::kXRawBytes);
   char* frag = base + L::kFragOff + buf * L::kFragBytes;
-  int* fexp = reinterpret_cast<int*>(base + L::kExpOff) + buf * 32;
+  int* fexp = reinterpret_cast<int*>(base + L::kExpOff) + buf * L::kExpInts;
   constexpr int kLaneRows = MODE == kN2 ? 1 : NB;  // rows this lane converts
   int rows[kLaneRows];
 #pragma unroll
@@ -307,7 +310,7 @@ __device__ __forceinline__ void prep_chunk(char* base, int buf, int ngr,
     if (ex[i] == kNoExp) ex[i] = 0;  // zero rows: any scale
   }
   changed = __any_sync(0xffffffffu, changed);
-  if (lane == 0) fexp[16] = changed ? 1 : 0;
+  if (lane == 0) fexp[L::kExpFlag] = changed ? 1 : 0;
 
   for (int j = 0; j < ngr; ++j) {
 #pragma unroll
@@ -640,9 +643,9 @@ __device__ __forceinline__ bool consumer_loop(char* base, int nq, int w, unsigne
       break;
     }
     int en[LR::kN];
-    const bool changed = c == 0 || fexp[32 * b + 16] != 0;  // same for the whole warp
+    const bool changed = c == 0 || fexp[L::kExpInts * b + L::kExpFlag] != 0;  // whole warp
 #pragma unroll
-    for (int i = 0; i < LR::kN; ++i) en[i] = changed ? fexp[32 * b + LR::row(t, i)] : ex[i];
+    for (int i = 0; i < LR::kN; ++i) en[i] = changed ? fexp[L::kExpInts * b + LR::row(t, i)] : ex[i];
     if (c > 0 && changed) {
       // accumulators from chunk units 2^(ex - 14) to 2^(en - 14)
 #pragma unroll
