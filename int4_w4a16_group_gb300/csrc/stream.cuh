@@ -351,6 +351,7 @@ struct Acc {
 // warp's tiles c < CH/2 are gate tiles, c >= CH/2 the matching up tiles.
 template <int W, int CH, bool SWIGLU>
 __device__ __forceinline__ int tile_slot(int w, int c) {
+  static_assert(!SWIGLU || CH % 2 == 0, "a fused SwiGLU warp holds gate/up tile pairs");
   if constexpr (SWIGLU) {
     constexpr int H = CH / 2, TT = W * CH / 2;
     return c < H ? w * H + c : TT + w * H + (c - H);
